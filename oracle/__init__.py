@@ -1,0 +1,6 @@
+"""CPU oracle of the H2O eviction policy (test infrastructure; see h2o_oracle)."""
+from .h2o_oracle import (NEAR_TIE, PrefillResult, RowCache, RowTrace, StepLog, decode_step,
+                         default_scale, prefill, prefill_attention, prefill_select, run_row)
+
+__all__ = ["NEAR_TIE", "PrefillResult", "RowCache", "RowTrace", "StepLog", "decode_step",
+           "default_scale", "prefill", "prefill_attention", "prefill_select", "run_row"]
