@@ -1,0 +1,438 @@
+"""Benchmark of the H2O heavy-hitter KV-cache hot path on GB300.
+
+One step = the whole hot path over one batch of synthetic input: prefill of the
+prompt (causal attention, column-sum scores, top-h + recent selection,
+compaction into the cache) followed by every decode step of the workload
+(attention over the cache, score accumulation, eviction, slot overwrite), the
+decode steps replayed from one CUDA graph. The metric is decode tokens per
+second: batch x decode steps per step, divided by the step's time (prefill
+included).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+With --gpus N > 1 (launched by torchrun) every rank runs its own full-size
+batch (independent sequences; no collective on the data path) and the time is
+the maximum over ranks.
+
+--impl reference times the CPU oracle (fp64, one process per host core) on a
+bounded sample of rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import multiprocessing as mp
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import (WORKLOADS, decode_bytes_per_row_step, head_direction,  # noqa: E402
+                       prefill_flops_per_row, row_tokens)
+
+METRIC = "H2O decode tokens/s/GPU at 20% KV budget; achieved HBM GB/s vs peak"
+UNIT = "tokens/s"
+PREFILL_LAUNCHES = 4  # forward, column sums, select, gather
+
+
+# --------------------------------------------------------------------------- CPU oracle leg
+def _oracle_rows_timed(job):
+    """Pool worker: runs the oracle on a list of rows; returns the compute seconds."""
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    import oracle
+    from workloads import bf16_bits_to_f64
+
+    w, rows_bits = job
+    t0 = time.perf_counter()
+    for q, k, v in rows_bits:
+        oracle.run_row(bf16_bits_to_f64(q), bf16_bits_to_f64(k), bf16_bits_to_f64(v), w.prompt,
+                       w.steps, w.h, w.r, keep_sets=False)
+    return time.perf_counter() - t0
+
+
+def _sample_rows(w, n):
+    rng = np.random.default_rng(12345)
+    idx = rng.choice(w.batch * w.heads, size=min(n, w.batch * w.heads), replace=False)
+    return [(int(i) // w.heads, int(i) % w.heads) for i in sorted(idx)]
+
+
+class OracleTimer:
+    """Times the CPU oracle on sampled rows with one spawn process per core."""
+
+    def __init__(self, w, rows_per_core=2):
+        self.w = w
+        self.cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        self.pool = mp.get_context("spawn").Pool(self.cores)
+        rows = _sample_rows(w, rows_per_core * self.cores)
+        self.rows = rows
+        bits = [row_tokens(w, 0, b, j, head_direction(w, 0, j)) for b, j in rows]
+        self.jobs = [(w, bits[i::self.cores]) for i in range(self.cores) if bits[i::self.cores]]
+
+    def run_once(self):
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_rows_timed, self.jobs, chunksize=1)
+        wall = time.perf_counter() - t0
+        tokens = len(self.rows) / self.w.heads * self.w.steps  # one token = all heads of a sequence
+        return tokens / wall, wall
+
+    def describe(self):
+        w = self.w
+        return (f"{len(self.rows)} of {w.batch * w.heads} (batch, head) rows of {w.name}, each a full "
+                f"prefill of {w.prompt} tokens plus {w.steps} decode steps; tokens counted as "
+                f"rows / heads x steps")
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = max(smax, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- helpers
+def _peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def _profiled_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current source of the kernel (its sha256 is recorded in the summary)."""
+    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}.md")
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not (m and b):
+        return None
+    src = open(os.path.join(ROOT, "h2o_heavy_hitter_gb300", "csrc", kernel_file), "rb").read()
+    if hashlib.sha256(src).hexdigest() != m.group(1):
+        return None
+    return float(b.group(1))
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args, w):
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return
+    timer = OracleTimer(w, rows_per_core=1)
+    try:
+        for _ in range(args.warmup):
+            timer.run_once()
+        vals, walls = [], []
+        for _ in range(args.steps):
+            v, wall = timer.run_once()
+            vals.append(v)
+            walls.append(wall)
+    finally:
+        timer.close()
+    value = float(len(timer.rows) / w.heads * w.steps * args.steps / sum(walls))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(walls) / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": timer.cores, "kind": "oracle",
+                         "sample": timer.describe()},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(w):
+    return {"workload": w.name, "layers": w.layers, "batch": w.batch, "heads": w.heads,
+            "head_dim": w.head_dim, "prompt": w.prompt, "decode_steps": w.steps, "h": w.h, "r": w.r,
+            "zipf_alpha": w.alpha,
+            "step": f"prefill of {w.prompt} tokens + {w.steps} decode steps (CUDA graph)",
+            "tokens_per_step": w.batch * w.steps,
+            "l2": "inputs larger than L2 (prompt Q/K/V read every step); the decode cache stays "
+                  "L2-resident across the decode steps of a step",
+            "parallelism": "one replica per GPU (independent batches)"}
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args, w):
+    import torch
+
+    ws, rank, local = _dist_env()
+    timer = OracleTimer(w) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
+    if ws > 1 and rank == 0 and not args.no_cpu_baseline:
+        timer = OracleTimer(w)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    from __graft_entry__ import build
+    build()
+    import h2o_heavy_hitter_gb300 as h2o
+
+    B, H, d, T, S = w.batch, w.heads, w.head_dim, w.prompt, w.steps
+    N = w.tokens
+    # Inputs: each rank draws its own layer seed (independent batches).
+    t0 = time.perf_counter()
+    bits = np.empty((3, B, H, N, d), dtype=np.uint16)
+    dirs = [head_direction(w, rank, j) for j in range(H)]
+    for b in range(B):
+        for j in range(H):
+            q, k, v = row_tokens(w, rank, b, j, dirs[j])
+            bits[0, b, j], bits[1, b, j], bits[2, b, j] = q, k, v
+    gen_s = time.perf_counter() - t0
+
+    def host(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+
+    hp = [host(bits[i][:, :, :T]).pin_memory() for i in range(3)]  # prompt [B,H,T,d]
+    hs = [host(bits[i][:, :, T:].transpose(2, 0, 1, 3)).pin_memory() for i in range(3)]  # [S,B,H,d]
+    dp = [x.to(dev) for x in hp]
+    ds = [x.to(dev) for x in hs]
+    pre_out = torch.empty((B, H, T, d), dtype=torch.float32, device=dev)
+    dec_out = torch.empty((S, B, H, d), dtype=torch.float32, device=dev)
+    h_pre_out = torch.empty(pre_out.shape, dtype=torch.float32).pin_memory()
+    h_dec_out = torch.empty(dec_out.shape, dtype=torch.float32).pin_memory()
+
+    ctx = h2o.h2o_create(1, B, H, d, w.h, w.r)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        h2o.h2o_prefill(ctx, 0, *dp, out=pre_out)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for s in range(S):
+                h2o.h2o_decode_step(ctx, 0, ds[0][s], ds[1][s], ds[2][s], dec_out[s])
+    torch.cuda.synchronize()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        h2o.h2o_prefill(ctx, 0, *dp, out=pre_out)
+        if ev is not None:
+            ev[1].record(stream)
+        graph.replay()
+        if ev is not None:
+            ev[2].record(stream)
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    torch.cuda.synchronize()
+
+    # ---- device-resident timed region
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    elapsed_ms = start.elapsed_time(end)
+    if pg is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    prefill_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    decode_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+
+    # ---- end-to-end through the public API with host buffers
+    h2d = sum(x.numel() * 2 for x in hp + hs)
+    d2h = (pre_out.numel() + dec_out.numel()) * 4
+
+    def e2e_step():
+        for dst, src in zip(dp, hp):
+            dst.copy_(src, non_blocking=True)
+        for dst, src in zip(ds, hs):
+            dst.copy_(src, non_blocking=True)
+        step()
+        h_pre_out.copy_(pre_out, non_blocking=True)
+        h_dec_out.copy_(dec_out, non_blocking=True)
+
+    e2e_steps = max(3, args.steps // 4)
+    with torch.cuda.stream(stream):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if pg is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # ---- decode launches with L2 flushed before each (HBM-cold reference point)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ctx_l2 = h2o.h2o_create(1, B, H, d, w.h, w.r)
+    with torch.cuda.stream(stream):
+        h2o.h2o_prefill(ctx_l2, 0, *dp, out=pre_out)
+    cold = []
+    n_cold = min(S, 64)
+    with torch.cuda.stream(stream):
+        for s in range(n_cold):
+            flush.fill_(s & 0xff)
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            h2o.h2o_decode_step(ctx_l2, 0, ds[0][s], ds[1][s], ds[2][s], dec_out[s])
+            b_.record(stream)
+            cold.append((a, b_))
+    torch.cuda.synchronize()
+    cold_ms = float(np.mean([a.elapsed_time(b_) for a, b_ in cold[1:]]))
+    h2o.h2o_sync_check(ctx_l2)
+    ctx_l2.close()
+    h2o.h2o_sync_check(ctx)
+    ctx.close()
+
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+
+    peaks, peak_kind = _peaks()
+    rows = B * H
+    bytes_per_launch = decode_bytes_per_row_step(w.k, d) * rows
+    dec_launch_ms = decode_ms / S  # graph replay: launch gaps included
+    achieved = bytes_per_launch / (dec_launch_ms * 1e-3) / 1e9
+    achieved_cold = bytes_per_launch / (cold_ms * 1e-3) / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    pflops = prefill_flops_per_row(T, d) * rows
+    pre_tflops = pflops / (prefill_ms * 1e-3) / 1e12
+    tokens = B * S * args.steps * ws
+    value = tokens / (elapsed_ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) q/k/v plus a power-law shared key direction per head; no weights",
+        "config": _config(w),
+        "roofline": {"kernel": "h2o decode_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": _profiled_traffic("decode.cu", w.name),
+                     "bytes_per_launch": bytes_per_launch,
+                     "launch_ms": dec_launch_ms,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "achieved_l2_flushed": achieved_cold, "frac_l2_flushed": achieved_cold / hbm,
+                     "launch_ms_l2_flushed": cold_ms},
+        "phases": {"prefill_ms": prefill_ms, "decode_ms": decode_ms,
+                   "prefill_tokens_per_s": B * T / (prefill_ms * 1e-3),
+                   "prefill_tflops": pre_tflops,
+                   "prefill_frac_bf16": pre_tflops / float(peaks["bf16_tflops"]),
+                   "decode_only_tokens_per_s": B * S / (decode_ms * 1e-3),
+                   "input_generation_s": gen_s},
+        "e2e": {"value": B * S * e2e_steps * ws / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": (PREFILL_LAUNCHES + S) * args.steps,
+        "clocks": clk,
+    }
+    if timer is not None:
+        v, wall = timer.run_once()
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": timer.cores, "kind": "oracle",
+                                "sample": timer.describe(), "wall_s": wall}
+        timer.close()
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="opt-6.7b-layer", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

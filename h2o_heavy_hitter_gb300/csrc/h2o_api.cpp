@@ -1,0 +1,316 @@
+// C ABI of the H2O heavy-hitter KV-cache library (declared in include/h2o.h).
+//
+// Host side only: argument checks, the per-layer state machine, cache
+// allocation from PyTorch's CUDA caching allocator, and kernel launches on the
+// current PyTorch stream. Every step of the policy runs in the CUDA kernels.
+#include "h2o.h"
+
+#include <c10/cuda/CUDACachingAllocator.h>
+#include <c10/cuda/CUDAFunctions.h>
+#include <c10/cuda/CUDAStream.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_error;
+
+int fail(int code, const std::string& msg) {
+  g_error = msg;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(H2O_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+cudaStream_t current_stream() { return c10::cuda::getCurrentCUDAStream().stream(); }
+
+int env_int(const char* name) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : 0;
+}
+
+// One device allocation from PyTorch's caching allocator, freed on scope exit.
+struct Scratch {
+  void* p = nullptr;
+  explicit Scratch(size_t bytes, cudaStream_t s) {
+    if (bytes) p = c10::cuda::CUDACachingAllocator::raw_alloc_with_stream(bytes, s);
+  }
+  ~Scratch() {
+    if (p) c10::cuda::CUDACachingAllocator::raw_delete(p);
+  }
+  Scratch(const Scratch&) = delete;
+  Scratch& operator=(const Scratch&) = delete;
+};
+
+}  // namespace
+
+struct h2o_ctx {
+  int layers, batch, heads, d, h, r, k, rows;
+  int device;
+  size_t kv_elems_per_layer;  // rows * k * d
+  void* base = nullptr;       // single cache allocation
+  uint16_t* K = nullptr;
+  uint16_t* V = nullptr;
+  float* score = nullptr;
+  int32_t* pos = nullptr;
+  int32_t* meta = nullptr;
+  int32_t* err = nullptr;     // device error word
+  std::vector<int> prompt_len;  // per layer: -1 until prefilled
+  h2o::DecodeConfig dcfg{};
+
+  void* layer_K(int l) const { return K + static_cast<size_t>(l) * kv_elems_per_layer; }
+  void* layer_V(int l) const { return V + static_cast<size_t>(l) * kv_elems_per_layer; }
+  float* layer_score(int l) const { return score + static_cast<size_t>(l) * rows * k; }
+  int32_t* layer_pos(int l) const { return pos + static_cast<size_t>(l) * rows * k; }
+  int32_t* layer_meta(int l) const { return meta + static_cast<size_t>(l) * rows * 4; }
+};
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int check_layer(const h2o_ctx* c, int layer) {
+  if (!c) return fail(H2O_EINVAL, "null context");
+  if (layer < 0 || layer >= c->layers) return fail(H2O_EINVAL, "layer out of range");
+  return H2O_OK;
+}
+
+int run_attention(const void* Q, const void* K, const void* V, int rows, int T, int d, float* out,
+                  float* colsum, int32_t* err, cudaStream_t s) {
+  Scratch lse(static_cast<size_t>(rows) * T * sizeof(float), s);
+  cudaError_t e = h2o::prefill_forward(Q, K, V, rows, T, d, out, static_cast<float*>(lse.p), err, s);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill forward launch");
+  e = h2o::prefill_colsum(Q, K, static_cast<float*>(lse.p), rows, T, d, colsum, err, s);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill column-sum launch");
+  return H2O_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* h2o_last_error(void) { return g_error.c_str(); }
+
+int h2o_create(int layers, int batch, int heads, int head_dim, int h, int r, h2o_ctx** out) {
+  if (!out) return fail(H2O_EINVAL, "null output pointer");
+  *out = nullptr;
+  if (layers < 1 || batch < 1 || heads < 1) return fail(H2O_EINVAL, "layers, batch and heads must be >= 1");
+  if (head_dim != 64 && head_dim != 128) return fail(H2O_EINVAL, "head_dim must be 64 or 128");
+  if (h < 0 || r < 0 || h + r < 1 || h + r > H2O_MAX_K)
+    return fail(H2O_EINVAL, "need h >= 0, r >= 0 and 1 <= h + r <= H2O_MAX_K");
+  const long rows_l = static_cast<long>(batch) * heads;
+  if (rows_l > (1L << 30)) return fail(H2O_EINVAL, "batch * heads too large");
+
+  auto* c = new h2o_ctx();
+  c->layers = layers;
+  c->batch = batch;
+  c->heads = heads;
+  c->d = head_dim;
+  c->h = h;
+  c->r = r;
+  c->k = h + r;
+  c->rows = static_cast<int>(rows_l);
+  c->prompt_len.assign(layers, -1);
+  try {
+    c->device = c10::cuda::current_device();
+  } catch (const std::exception& ex) {
+    delete c;
+    return fail(H2O_ECUDA, std::string("no CUDA device: ") + ex.what());
+  }
+  int sms = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device);
+  if (e != cudaSuccess) {
+    delete c;
+    return cuda_fail(e, "cudaDeviceGetAttribute");
+  }
+
+  const size_t L = layers, R = c->rows, K = c->k, D = head_dim;
+  c->kv_elems_per_layer = R * K * D;
+  const size_t kv_bytes = align_up(L * R * K * D * 2, 256);
+  const size_t sc_bytes = align_up(L * R * K * 4, 256);
+  const size_t meta_bytes = align_up(L * R * 16, 256);
+  const size_t total = 2 * kv_bytes + 2 * sc_bytes + meta_bytes + 256;
+  cudaStream_t s = current_stream();
+  try {
+    c->base = c10::cuda::CUDACachingAllocator::raw_alloc_with_stream(total, s);
+  } catch (const std::exception& ex) {
+    delete c;
+    return fail(H2O_ENOMEM, std::string("cache allocation failed: ") + ex.what());
+  }
+  char* p = static_cast<char*>(c->base);
+  c->K = reinterpret_cast<uint16_t*>(p);
+  p += kv_bytes;
+  c->V = reinterpret_cast<uint16_t*>(p);
+  p += kv_bytes;
+  c->score = reinterpret_cast<float*>(p);
+  p += sc_bytes;
+  c->pos = reinterpret_cast<int32_t*>(p);
+  p += sc_bytes;
+  c->meta = reinterpret_cast<int32_t*>(p);
+  p += meta_bytes;
+  c->err = reinterpret_cast<int32_t*>(p);
+
+  e = cudaMemsetAsync(c->err, 0, sizeof(int32_t), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->K, 0, 2 * kv_bytes, s);
+  for (int l = 0; l < layers && e == cudaSuccess; ++l)
+    e = h2o::cache_reset(c->rows, c->k, c->layer_score(l), c->layer_pos(l), c->layer_meta(l), s);
+  if (e != cudaSuccess) {
+    h2o_destroy(c);
+    return cuda_fail(e, "cache initialisation");
+  }
+  c->dcfg = h2o::decode_config(c->rows, c->k, c->d, sms, env_int("H2O_DECODE_CLUSTER"),
+                               env_int("H2O_DECODE_STAGES"));
+  e = h2o::decode_prepare(c->dcfg, c->d);
+  if (e != cudaSuccess) {
+    h2o_destroy(c);
+    return cuda_fail(e, "decode kernel attributes");
+  }
+  *out = c;
+  return H2O_OK;
+}
+
+void h2o_destroy(h2o_ctx* c) {
+  if (!c) return;
+  if (c->base) {
+    cudaStreamSynchronize(current_stream());
+    c10::cuda::CUDACachingAllocator::raw_delete(c->base);
+  }
+  delete c;
+}
+
+int h2o_prefill(h2o_ctx* c, int layer, const void* Q, const void* K, const void* V, int T,
+                float* out) {
+  if (int rc = check_layer(c, layer)) return rc;
+  if (T < 0 || T > H2O_MAX_T) return fail(H2O_EINVAL, "T out of range");
+  cudaStream_t s = current_stream();
+  cudaError_t e;
+  if (T == 0) {
+    e = h2o::cache_reset(c->rows, c->k, c->layer_score(layer), c->layer_pos(layer),
+                         c->layer_meta(layer), s);
+    if (e != cudaSuccess) return cuda_fail(e, "cache reset");
+    c->prompt_len[layer] = 0;
+    return H2O_OK;
+  }
+  if (!Q || !K || !V || !out) return fail(H2O_EINVAL, "null Q, K, V or out");
+  try {
+    Scratch colsum(static_cast<size_t>(c->rows) * T * sizeof(float), s);
+    int rc = run_attention(Q, K, V, c->rows, T, c->d, out, static_cast<float*>(colsum.p), c->err, s);
+    if (rc) return rc;
+    e = h2o::prefill_select(static_cast<float*>(colsum.p), c->rows, T, c->h, c->r,
+                            c->layer_score(layer), c->layer_pos(layer), c->layer_meta(layer), s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill select launch");
+    e = h2o::prefill_gather(K, V, c->rows, T, c->d, c->k, c->layer_pos(layer), c->layer_K(layer),
+                            c->layer_V(layer), s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill gather launch");
+  } catch (const std::exception& ex) {
+    return fail(H2O_ENOMEM, std::string("prefill scratch allocation failed: ") + ex.what());
+  }
+  c->prompt_len[layer] = T;
+  return H2O_OK;
+}
+
+int h2o_prefill_attention(const void* Q, const void* K, const void* V, int rows, int T,
+                          int head_dim, float* out, float* score) {
+  if (rows < 0 || T < 0 || T > H2O_MAX_T) return fail(H2O_EINVAL, "rows or T out of range");
+  if (head_dim != 64 && head_dim != 128) return fail(H2O_EINVAL, "head_dim must be 64 or 128");
+  if (static_cast<long>(rows) * T == 0) return H2O_OK;
+  if (!Q || !K || !V || !out || !score) return fail(H2O_EINVAL, "null pointer");
+  try {
+    return run_attention(Q, K, V, rows, T, head_dim, out, score, nullptr, current_stream());
+  } catch (const std::exception& ex) {
+    return fail(H2O_ENOMEM, std::string("scratch allocation failed: ") + ex.what());
+  }
+}
+
+int h2o_decode_step(h2o_ctx* c, int layer, const void* q, const void* k_new, const void* v_new,
+                    float* out) {
+  if (int rc = check_layer(c, layer)) return rc;
+  if (!q || !k_new || !v_new || !out) return fail(H2O_EINVAL, "null q, k_new, v_new or out");
+  if (c->prompt_len[layer] < 0) return fail(H2O_ESTATE, "decode step before prefill of this layer");
+  h2o::DecodeArgs a{};
+  a.Kc = c->layer_K(layer);
+  a.Vc = c->layer_V(layer);
+  a.score = c->layer_score(layer);
+  a.pos = c->layer_pos(layer);
+  a.meta = c->layer_meta(layer);
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.out = out;
+  a.err = c->err;
+  a.k = c->k;
+  a.r = c->r;
+  a.chunk = c->dcfg.chunk;
+  a.qscale = h2o::kLog2e / std::sqrt(static_cast<float>(c->d));
+  cudaError_t e = h2o::decode_launch(a, c->dcfg, c->rows, c->d, current_stream());
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return H2O_OK;
+}
+
+int h2o_cache_positions(h2o_ctx* c, int layer, int32_t* host_pos) {
+  if (int rc = check_layer(c, layer)) return rc;
+  if (!host_pos) return fail(H2O_EINVAL, "null host buffer");
+  cudaStream_t s = current_stream();
+  cudaError_t e = cudaMemcpyAsync(host_pos, c->layer_pos(layer),
+                                  static_cast<size_t>(c->rows) * c->k * sizeof(int32_t),
+                                  cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e, "positions copy");
+  return h2o_sync_check(c);
+}
+
+int h2o_last_evicted(h2o_ctx* c, int layer, int32_t* host_pos) {
+  if (int rc = check_layer(c, layer)) return rc;
+  if (!host_pos) return fail(H2O_EINVAL, "null host buffer");
+  cudaStream_t s = current_stream();
+  cudaError_t e = cudaMemcpy2DAsync(host_pos, sizeof(int32_t), c->layer_meta(layer) + 2,
+                                    4 * sizeof(int32_t), sizeof(int32_t), c->rows,
+                                    cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e, "evicted-position copy");
+  return h2o_sync_check(c);
+}
+
+int h2o_cache_view(h2o_ctx* c, int layer, void** K, void** V, float** score, int32_t** pos,
+                   int32_t** meta) {
+  if (int rc = check_layer(c, layer)) return rc;
+  if (K) *K = c->layer_K(layer);
+  if (V) *V = c->layer_V(layer);
+  if (score) *score = c->layer_score(layer);
+  if (pos) *pos = c->layer_pos(layer);
+  if (meta) *meta = c->layer_meta(layer);
+  return H2O_OK;
+}
+
+int h2o_cache_dims(h2o_ctx* c, int* k, int* rows) {
+  if (!c) return fail(H2O_EINVAL, "null context");
+  if (k) *k = c->k;
+  if (rows) *rows = c->rows;
+  return H2O_OK;
+}
+
+int h2o_sync_check(h2o_ctx* c) {
+  if (!c) return fail(H2O_EINVAL, "null context");
+  cudaStream_t s = current_stream();
+  int32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, c->err, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
+  if (word != 0) {
+    cudaMemsetAsync(c->err, 0, sizeof(int32_t), s);
+    char buf[96];
+    std::snprintf(buf, sizeof(buf), "device error word 0x%x (1 = wait timeout, 2 = bad state)", word);
+    return fail(H2O_EDEVICE, buf);
+  }
+  return H2O_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,221 @@
+// Prefill selection and compaction of the H2O policy (H2O: Heavy-Hitter
+// Oracle ..., summary page, appendix A: Pseudocode and System Details).
+//
+// select:  per row, keep the r most recent prompt tokens and the h other
+//          tokens with the largest (score, position) keys (every token when
+//          T <= h + r). The h-th largest key is found by an MSB-first radix
+//          select over the fp32 score bits (scores are non-negative, so their
+//          bit patterns order like the values); ties at the boundary score
+//          keep the later positions. The kept positions are compacted in
+//          ascending order into the row's cache slots with block-wide scans.
+// gather:  copy the K/V rows of the kept positions into their slots.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace h2o {
+namespace {
+
+constexpr int kSelectThreads = 1024;
+
+// Block-wide exclusive scan of one int per thread; *total gets the sum.
+__device__ __forceinline__ int block_exclusive_scan(int x, int* wsum, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = lane < nw ? wsum[lane] : 0;
+    int vi = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, vi, off);
+      if (lane >= off) vi += y;
+    }
+    wsum[lane] = vi - v;
+    if (lane == 31) wsum[32] = vi;
+  }
+  __syncthreads();
+  const int r = wsum[warp] + incl - x;
+  *total = wsum[32];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kSelectThreads) select_kernel(const float* __restrict__ colsum,
+                                                               int T, int h, int r, int k,
+                                                               float* __restrict__ score,
+                                                               int32_t* __restrict__ pos,
+                                                               int32_t* __restrict__ meta) {
+  __shared__ unsigned hist[256];
+  __shared__ int wsum[33];
+  __shared__ unsigned s_prefix;
+  __shared__ int s_rank;
+  const int row = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+  const float* cs = colsum + static_cast<size_t>(row) * T;
+  float* sc = score + static_cast<size_t>(row) * k;
+  int32_t* ps = pos + static_cast<size_t>(row) * k;
+
+  const bool keep_all = T <= k;
+  const int n_cand = keep_all ? 0 : T - r;
+  // Keep candidate p iff bits(score_p) > tau, or == tau and p is not among the
+  // first `skip` candidates holding that exact score.
+  unsigned tau = 0xffffffffu;
+  int skip = 0x7fffffff;
+  if (!keep_all && h > 0) {
+    unsigned prefix = 0, mask = 0;
+    int rank = n_cand - h;  // index, in ascending (score, position) order, of the smallest kept key
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += nt) hist[i] = 0;
+      __syncthreads();
+      for (int p = tid; p < n_cand; p += nt) {
+        const unsigned u = __float_as_uint(cs[p]);
+        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        int cum = 0;
+        for (int b = 0; b < 256; ++b) {
+          const int c = static_cast<int>(hist[b]);
+          if (cum + c > rank) {
+            s_prefix = prefix | (static_cast<unsigned>(b) << shift);
+            s_rank = rank - cum;
+            break;
+          }
+          cum += c;
+        }
+      }
+      __syncthreads();
+      prefix = s_prefix;
+      rank = s_rank;
+      mask |= 0xffu << shift;
+    }
+    tau = prefix;
+    skip = rank;
+  }
+
+  const int seg = (T + nt - 1) / nt;
+  const int p0 = min(T, tid * seg), p1 = min(T, p0 + seg);
+  int eq = 0;
+  if (!keep_all && h > 0)
+    for (int p = p0; p < min(p1, n_cand); ++p) eq += __float_as_uint(cs[p]) == tau;
+  int dummy;
+  const int eq_base = block_exclusive_scan(eq, wsum, &dummy);
+
+  auto keep = [&](int p, int& e) -> bool {
+    if (keep_all || p >= n_cand) return true;
+    if (h == 0) return false;
+    const unsigned u = __float_as_uint(cs[p]);
+    if (u > tau) return true;
+    if (u == tau) return (e++) >= skip;
+    return false;
+  };
+  int kept = 0;
+  {
+    int e = eq_base;
+    for (int p = p0; p < p1; ++p) kept += keep(p, e);
+  }
+  int total;
+  int s = block_exclusive_scan(kept, wsum, &total);
+  {
+    int e = eq_base;
+    for (int p = p0; p < p1; ++p)
+      if (keep(p, e)) {
+        ps[s] = p;
+        sc[s] = cs[p];
+        ++s;
+      }
+  }
+  for (int j = total + tid; j < k; j += nt) {
+    ps[j] = -1;
+    sc[j] = 0.f;
+  }
+  if (tid == 0) {
+    int32_t* mr = meta + static_cast<size_t>(row) * 4;
+    mr[0] = total;
+    mr[1] = T;
+    mr[2] = -1;
+    mr[3] = 0;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __restrict__ K,
+                                                    const __nv_bfloat16* __restrict__ V, int T,
+                                                    int k, const int32_t* __restrict__ pos,
+                                                    __nv_bfloat16* __restrict__ Kc,
+                                                    __nv_bfloat16* __restrict__ Vc) {
+  constexpr int CH = D / 8;  // 16-byte chunks per row
+  const int row = blockIdx.x;
+  const int slot = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (slot >= k) return;
+  const int p = pos[static_cast<size_t>(row) * k + slot];
+  if (p < 0) return;
+  const size_t src = (static_cast<size_t>(row) * T + p) * D;
+  const size_t dst = (static_cast<size_t>(row) * k + slot) * D;
+  for (int c = lane; c < 2 * CH; c += 32) {
+    const bool isv = c >= CH;
+    const int cc = isv ? c - CH : c;
+    const uint4 v = *reinterpret_cast<const uint4*>((isv ? V : K) + src + cc * 8);
+    *reinterpret_cast<uint4*>((isv ? Vc : Kc) + dst + cc * 8) = v;
+  }
+}
+
+__global__ void reset_kernel(int rows, int k, float* __restrict__ score, int32_t* __restrict__ pos,
+                             int32_t* __restrict__ meta) {
+  const size_t n = static_cast<size_t>(rows) * k;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    pos[i] = -1;
+    score[i] = 0.f;
+    if (i < static_cast<size_t>(rows)) {
+      meta[4 * i + 0] = 0;
+      meta[4 * i + 1] = 0;
+      meta[4 * i + 2] = -1;
+      meta[4 * i + 3] = 0;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t prefill_select(const float* colsum, int rows, int T, int h, int r, float* score,
+                           int32_t* pos, int32_t* meta, cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  select_kernel<<<rows, kSelectThreads, 0, stream>>>(colsum, T, h, r, h + r, score, pos, meta);
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_gather(const void* K, const void* V, int rows, int T, int d, int k,
+                           const int32_t* pos, void* Kc, void* Vc, cudaStream_t stream) {
+  if (rows == 0 || T == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>((k + 7) / 8));
+  auto kk = static_cast<const __nv_bfloat16*>(K);
+  auto vv = static_cast<const __nv_bfloat16*>(V);
+  auto kc = static_cast<__nv_bfloat16*>(Kc);
+  auto vc = static_cast<__nv_bfloat16*>(Vc);
+  if (d == 128)
+    gather_kernel<128><<<grid, 256, 0, stream>>>(kk, vv, T, k, pos, kc, vc);
+  else
+    gather_kernel<64><<<grid, 256, 0, stream>>>(kk, vv, T, k, pos, kc, vc);
+  return cudaGetLastError();
+}
+
+cudaError_t cache_reset(int rows, int k, float* score, int32_t* pos, int32_t* meta,
+                        cudaStream_t stream) {
+  const size_t n = static_cast<size_t>(rows) * k;
+  if (n == 0) return cudaSuccess;
+  const unsigned blocks = static_cast<unsigned>(std::min<size_t>((n + 255) / 256, 4096));
+  reset_kernel<<<blocks, 256, 0, stream>>>(rows, k, score, pos, meta);
+  return cudaGetLastError();
+}
+
+}  // namespace h2o

@@ -1,0 +1,177 @@
+/*
+ * h2o.h - C ABI of the GB300 (sm_103a) H2O heavy-hitter KV-cache library.
+ *
+ * Sources (page title and section):
+ *   [H2O] "H2O: Heavy-Hitter Oracle for Efficient Generative Inference of Large
+ *         Language Models", section-by-section summary page of arXiv 2306.14048v3.
+ *
+ * The policy keeps, for every (layer, batch row, head) "row", at most
+ * k = h + r cached tokens: h heavy hitters and the r most recent tokens
+ * ([H2O] A, System Details). A token's accumulated score is the running sum of
+ * the softmax probabilities it has received ([H2O] 1, 3.2). At most one token is
+ * evicted per decoding step and the cache never exceeds k ([H2O] TL;DR, 2).
+ *
+ * Conventions shared by every entry point
+ *   - Return value: H2O_OK (0) on success, a negative H2O_E* code on failure.
+ *     h2o_last_error() then returns a message for the calling thread. No entry
+ *     point traps or aborts; device kernels never trap. Bounded device waits
+ *     that give up set a device error word that h2o_sync_check() reports.
+ *   - Device pointers are CUDA device addresses on the current device; host
+ *     pointers are ordinary CPU memory. Every buffer passed in stays owned by
+ *     the caller and is only accessed by work the call enqueues.
+ *   - All device work is enqueued, asynchronously, on the calling thread's
+ *     current PyTorch CUDA stream (c10::cuda::getCurrentCUDAStream()). The
+ *     caller must have initialised PyTorch's CUDA state on that device
+ *     (torch.cuda.init() or any CUDA tensor). Only h2o_cache_positions,
+ *     h2o_last_evicted and h2o_sync_check synchronise with the host.
+ *   - The library owns the cache. It allocates it from PyTorch's CUDA caching
+ *     allocator and frees it in h2o_destroy. PyTorch serves for nothing else.
+ *   - Layouts: Q, K, V of a prompt are bf16, contiguous [batch, heads, T, d];
+ *     decode inputs q, k_new, v_new are bf16, contiguous [batch, heads, d];
+ *     outputs are fp32 in the same layouts. head_dim d is 64 or 128. Logits
+ *     are scaled by 1/sqrt(d).
+ *   - Position t counts tokens of a row from 0: prompt tokens are 0 .. T-1 and
+ *     decode step s processes position T + s.
+ */
+#ifndef H2O_H
+#define H2O_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define H2O_OK 0
+#define H2O_EINVAL (-1)  /* bad argument (null pointer, size out of range, layer out of range) */
+#define H2O_ESTATE (-2)  /* call not valid in the current state (decode before prefill) */
+#define H2O_ENOMEM (-3)  /* device allocation failed */
+#define H2O_ECUDA (-4)   /* a CUDA runtime call or kernel launch failed */
+#define H2O_EDEVICE (-5) /* a kernel reported an error through the device error word */
+
+#define H2O_MAX_T (1 << 20)  /* longest prompt accepted by h2o_prefill */
+#define H2O_MAX_K 32768      /* largest budget h + r accepted by h2o_create */
+
+typedef struct h2o_ctx h2o_ctx; /* opaque; created by h2o_create, freed by h2o_destroy */
+
+/*
+ * h2o_create - allocate the cache of a model: `layers` layers of batch x heads
+ * rows, each with a budget of h heavy-hitter plus r recent tokens ([H2O] A,
+ * System Details: preallocated cache with a heavy-hitter and a recent region).
+ *
+ * Per layer the cache holds, for rows = batch * heads and k = h + r slots:
+ *   K, V   bf16  [rows][k][d]   cached keys / values, slot-indexed
+ *   score  fp32  [rows][k]      accumulated attention score of each slot
+ *   pos    int32 [rows][k]      token position held by each slot (-1 = empty)
+ *   meta   int32 [rows][4]      {filled slots, next position t, last evicted position (-1 none), 0}
+ * Slots [0, filled) are occupied; slot order carries no meaning.
+ *
+ * Arguments: layers >= 1, batch >= 1, heads >= 1, head_dim in {64, 128},
+ * h >= 0, r >= 0, 1 <= h + r <= H2O_MAX_K. *out receives the new context.
+ * Errors: H2O_EINVAL, H2O_ENOMEM, H2O_ECUDA. On error *out is set to NULL.
+ */
+int h2o_create(int layers, int batch, int heads, int head_dim, int h, int r, h2o_ctx** out);
+
+/* h2o_destroy - free the cache and the context. Waits for the context's
+ * stream work to finish first. NULL is accepted. */
+void h2o_destroy(h2o_ctx* ctx);
+
+/*
+ * h2o_prefill - prompt pass of one layer ([H2O] A, Pseudocode: a prompt of at
+ * least 2K tokens keeps K heavy hitters and K recent tokens).
+ *
+ * For every row: causal softmax attention of the T prompt queries over the
+ * prompt keys, written to out; the accumulated score of prompt token j is the
+ * column sum sum_{i >= j} P_ij of the causal probability matrix ([H2O] 3.2);
+ * the cache then holds the r most recent tokens T-r .. T-1 plus the h other
+ * tokens with the largest (score, position) keys, or every token if T <= h + r.
+ * Ties in score keep the later position. Retained tokens keep their column
+ * sums as accumulated scores. The layer's previous cache content is replaced.
+ *
+ * Q, K, V: device bf16 [batch, heads, T, d]; out: device fp32 [batch, heads, T, d].
+ * 0 <= T <= H2O_MAX_T; with T = 0 the pointers may be NULL and the layer is
+ * reset to an empty cache. Scratch (per-row log-sum-exp and column sums,
+ * 8 bytes per prompt token) comes from PyTorch's caching allocator on the
+ * current stream. Errors: H2O_EINVAL, H2O_ENOMEM, H2O_ECUDA.
+ */
+int h2o_prefill(h2o_ctx* ctx, int layer, const void* Q, const void* K, const void* V, int T,
+                float* out);
+
+/*
+ * h2o_decode_step - one generation step of one layer ([H2O] 4.1 and 2).
+ *
+ * For every row, with t its next position: append the new token (q, k_new,
+ * v_new); attend over the cached tokens plus the new one, writing
+ * out = sum_j p_j v_j with p = softmax(K q / sqrt(d)); add p_j to every cached
+ * token's accumulated score and give the new token score p_t; if the row now
+ * holds more than k tokens, evict the token with the smallest (score, position)
+ * among those at positions <= t - r (the r most recent, t included, are never
+ * evicted; with r = 0 the new token competes and may be dropped at once); the
+ * new token's K/V, position and score go into the freed slot, or into the next
+ * empty slot while the cache is not full.
+ *
+ * q, k_new, v_new: device bf16 [batch, heads, d]; out: device fp32 [batch, heads, d].
+ * Allocates nothing and never synchronises. The step position and fill count
+ * live in device memory and are advanced by the kernel, so the call can be
+ * captured in a CUDA graph and replayed. Errors: H2O_EINVAL, H2O_ESTATE (layer
+ * never prefilled), H2O_ECUDA.
+ */
+int h2o_decode_step(h2o_ctx* ctx, int layer, const void* q, const void* k_new, const void* v_new,
+                    float* out);
+
+/*
+ * h2o_prefill_attention - the attention part of prefill, without touching any
+ * cache: causal attention of `rows` independent rows of T tokens, the output
+ * and every token's column-sum score.
+ *
+ * Q, K, V: device bf16 [rows, T, d]; out: device fp32 [rows, T, d];
+ * score: device fp32 [rows, T]. Scratch (per-row log-sum-exp, 4 bytes per
+ * token) comes from PyTorch's caching allocator on the current stream.
+ * Errors: H2O_EINVAL, H2O_ENOMEM, H2O_ECUDA.
+ */
+int h2o_prefill_attention(const void* Q, const void* K, const void* V, int rows, int T,
+                          int head_dim, float* out, float* score);
+
+/*
+ * h2o_cache_positions - copy the positions held by every slot of one layer to
+ * host memory: host_pos int32 [batch * heads * k], row-major by (row, slot),
+ * -1 for empty slots. Synchronises the current stream.
+ * Errors: H2O_EINVAL, H2O_ECUDA, H2O_EDEVICE.
+ */
+int h2o_cache_positions(h2o_ctx* ctx, int layer, int32_t* host_pos);
+
+/*
+ * h2o_last_evicted - copy, per row, the position evicted by the layer's last
+ * decode step (-1 when the step evicted nothing): host_pos int32
+ * [batch * heads]. Synchronises the current stream.
+ * Errors: H2O_EINVAL, H2O_ECUDA, H2O_EDEVICE.
+ */
+int h2o_last_evicted(h2o_ctx* ctx, int layer, int32_t* host_pos);
+
+/*
+ * h2o_cache_view - device addresses of one layer's cache arrays (layouts as in
+ * h2o_create). The library keeps ownership; the addresses stay valid until
+ * h2o_destroy. A caller may write through them (between calls, on the same
+ * stream) to install a cache state; the fill count in meta must then match the
+ * occupied slots. Any output pointer may be NULL. Errors: H2O_EINVAL.
+ */
+int h2o_cache_view(h2o_ctx* ctx, int layer, void** K, void** V, float** score, int32_t** pos,
+                   int32_t** meta);
+
+/* h2o_cache_dims - k (slots per row) and rows (batch * heads) per layer. */
+int h2o_cache_dims(h2o_ctx* ctx, int* k, int* rows);
+
+/*
+ * h2o_sync_check - synchronise the current stream and report, then clear, the
+ * context's device error word. Errors: H2O_ECUDA, H2O_EDEVICE.
+ */
+int h2o_sync_check(h2o_ctx* ctx);
+
+/* h2o_last_error - message of the calling thread's last failed call ("" if none). */
+const char* h2o_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H2O_H */

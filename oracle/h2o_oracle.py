@@ -246,6 +246,7 @@ class RowTrace:
     evicted: list = field(default_factory=list)
     margins: list = field(default_factory=list)
     kept_after: list = field(default_factory=list)
+    scores_after: list = field(default_factory=list)
 
 
 def run_row(q_all, k_all, v_all, T: int, S: int, h: int, r: int,
@@ -265,4 +266,5 @@ def run_row(q_all, k_all, v_all, T: int, S: int, h: int, r: int,
         tr.margins.append(lg.margin)
         if keep_sets:
             tr.kept_after.append(c.pos.copy())
+            tr.scores_after.append(c.score.copy())
     return tr

@@ -1,0 +1,243 @@
+"""Lock-step parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Test support only. The oracle runs each checked row on its own (prefill then
+every decode step) in a spawn process pool, independently of the GPU; the GPU
+then runs the same workload and every step is compared:
+
+  * retained position sets and evicted positions must be equal, except at
+    steps where the oracle's relative margin between the evicted key and the
+    runner-up (or, at prefill, the smallest kept and the largest dropped
+    heavy-hitter score) is below 1e-4. Such near-ties are counted and the GPU
+    row is overwritten with the oracle's state (through h2o_cache_view) so the
+    runs stay comparable;
+  * outputs must be within 2e-2 max-abs and 2e-3 mean-abs of the oracle.
+
+Inputs come from the seeded generator. With ``tile=True`` only the checked
+rows are drawn and the GPU batch is filled by repeating them; every row is
+independent, so each GPU copy of a checked row must reproduce the oracle and
+the launch keeps the full-size shape.
+"""
+from __future__ import annotations
+
+import multiprocessing as mp
+import os
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+import oracle
+from workloads import Workload, bf16_bits_to_f64, head_direction, row_tokens
+
+MAX_ABS = 2e-2
+MEAN_ABS = 2e-3
+
+
+def _oracle_row(job):
+    """Runs the oracle on one row; returns compact per-step logs (pool worker)."""
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    w, layer, b, j, row_block = job
+    q, k, v = row_tokens(w, layer, b, j, head_direction(w, layer, j))
+    q, k, v = bf16_bits_to_f64(q), bf16_bits_to_f64(k), bf16_bits_to_f64(v)
+    tr = oracle.run_row(q, k, v, w.prompt, w.steps, w.h, w.r, row_block=row_block)
+    pre = tr.prefill
+    return {
+        "O": pre.O.astype(np.float32),
+        "colsum": pre.colsum,
+        "kept": pre.kept,
+        "kept_scores": pre.colsum[pre.kept],
+        "margin": pre.margin,
+        "outs": np.array(tr.outs, dtype=np.float64).reshape(w.steps, w.head_dim),
+        "evicted": np.array(tr.evicted, dtype=np.int64),
+        "margins": np.array(tr.margins, dtype=np.float64),
+        "kept_after": tr.kept_after,
+        "scores_after": tr.scores_after,
+    }
+
+
+def oracle_traces(w: Workload, layer: int, rows: list, workers: int | None = None,
+                  row_block: int | None = None) -> list:
+    jobs = [(w, layer, b, j, row_block) for (b, j) in rows]
+    if workers is None:
+        workers = min(len(jobs), max(1, (os.cpu_count() or 2) - 1))
+    if workers <= 1 or len(jobs) <= 1:
+        return [_oracle_row(jb) for jb in jobs]
+    with mp.get_context("spawn").Pool(workers) as pool:
+        return pool.map(_oracle_row, jobs, chunksize=1)
+
+
+@dataclass
+class Report:
+    rows: int = 0
+    steps: int = 0
+    evict_checks: int = 0
+    set_checks: int = 0
+    mismatches: list = field(default_factory=list)  # (step, row, gpu, oracle, margin) outside near-ties
+    near_ties: int = 0
+    near_tie_mismatches: int = 0
+    resyncs: int = 0
+    prefill_max_abs: float = 0.0
+    prefill_mean_abs: float = 0.0
+    decode_max_abs: float = 0.0
+    decode_mean_abs: float = 0.0
+    score_max_rel: float = 0.0
+
+    def ok(self) -> bool:
+        return (not self.mismatches and self.prefill_max_abs <= MAX_ABS
+                and self.prefill_mean_abs <= MEAN_ABS and self.decode_max_abs <= MAX_ABS
+                and self.decode_mean_abs <= MEAN_ABS)
+
+
+def _to_bf16(bits: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def _resync_row(view, gpu_row: int, pos: np.ndarray, scores: np.ndarray, k_bits, v_bits, k: int,
+                t_next: int):
+    """Overwrite one GPU row with the oracle's retained set (slot order = ascending position)."""
+    n = len(pos)
+    dev = view["pos"].device
+    pos_full = np.full(k, -1, dtype=np.int32)
+    pos_full[:n] = pos
+    sc_full = np.zeros(k, dtype=np.float32)
+    sc_full[:n] = scores
+    view["pos"][gpu_row] = torch.from_numpy(pos_full).to(dev)
+    view["score"][gpu_row] = torch.from_numpy(sc_full).to(dev)
+    view["K"][gpu_row, :n] = _to_bf16(k_bits[pos], dev)
+    view["V"][gpu_row, :n] = _to_bf16(v_bits[pos], dev)
+    view["meta"][gpu_row] = torch.tensor([n, t_next, -1, 0], dtype=torch.int32, device=dev)
+
+
+def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool = False,
+               set_check_every: int = 1, workers: int | None = None,
+               row_block: int | None = None, traces: list | None = None) -> Report:
+    """Runs one layer of workload ``w`` on the GPU and compares with the oracle.
+
+    ``rows``: (b, head) pairs checked against the oracle (default: all)."""
+    import h2o_heavy_hitter_gb300 as h2o
+
+    B, H, d, T, S, k = w.batch, w.heads, w.head_dim, w.prompt, w.steps, w.k
+    if rows is None:
+        rows = [(b, j) for b in range(B) for j in range(H)]
+    if traces is None:
+        traces = oracle_traces(w, layer, rows, workers, row_block)
+    dev = torch.device("cuda")
+    N = w.tokens
+
+    # GPU inputs [B, H, N, d] as bf16 bits.
+    row_bits = [row_tokens(w, layer, b, j, head_direction(w, layer, j)) for (b, j) in rows]
+    if tile:
+        src = [i % len(rows) for i in range(B * H)]
+        gpu_of = {}  # checked gpu row -> trace index (first copy)
+        for g, s in enumerate(src):
+            gpu_of.setdefault(s, g)
+        check = [(gpu_of[i], i) for i in range(len(rows))]
+        allq = np.stack([row_bits[s][0] for s in src]).reshape(B, H, N, d)
+        allk = np.stack([row_bits[s][1] for s in src]).reshape(B, H, N, d)
+        allv = np.stack([row_bits[s][2] for s in src]).reshape(B, H, N, d)
+        copies = np.array(src)
+    else:
+        from workloads import layer_tokens
+        if len(rows) == B * H:
+            allq = np.stack([x[0] for x in row_bits]).reshape(B, H, N, d)
+            allk = np.stack([x[1] for x in row_bits]).reshape(B, H, N, d)
+            allv = np.stack([x[2] for x in row_bits]).reshape(B, H, N, d)
+        else:
+            allq, allk, allv = layer_tokens(w, layer)
+        check = [(b * H + j, i) for i, (b, j) in enumerate(rows)]
+        copies = None
+    Qd, Kd, Vd = (_to_bf16(x, dev) for x in (allq, allk, allv))
+
+    rep = Report(rows=len(check), steps=S)
+    ctx = h2o.h2o_create(1, B, H, d, w.h, w.r)
+    try:
+        out = h2o.h2o_prefill(ctx, 0, Qd[:, :, :T].contiguous(), Kd[:, :, :T].contiguous(),
+                              Vd[:, :, :T].contiguous())
+        view = h2o.h2o_cache_view(ctx, 0)
+        gpu_rows = torch.tensor([g for g, _ in check], device=dev)
+        O = out.reshape(B * H, T, d)[gpu_rows].cpu().numpy().astype(np.float64)
+        errs = [np.abs(O[i] - traces[ti]["O"].astype(np.float64)) for i, (_, ti) in enumerate(check)]
+        if T:
+            rep.prefill_max_abs = float(max(e.max() for e in errs))
+            rep.prefill_mean_abs = float(np.mean([e.mean() for e in errs]))
+
+        pos = h2o.h2o_cache_positions(ctx, 0)
+        scores = view["score"].cpu().numpy()
+        for gi, (g, ti) in enumerate(check):
+            tr = traces[ti]
+            gp = np.sort(pos[g][pos[g] >= 0])
+            rep.set_checks += 1
+            if not np.array_equal(gp, tr["kept"]):
+                if tr["margin"] < oracle.NEAR_TIE:
+                    rep.near_tie_mismatches += 1
+                    rep.resyncs += 1
+                    b_, j_ = rows[ti]
+                    _, kb, vb = row_bits[ti]
+                    _resync_row(view, g, tr["kept"], tr["kept_scores"], kb, vb, k, T)
+                else:
+                    rep.mismatches.append((-1, g, gp.tolist(), tr["kept"].tolist(), tr["margin"]))
+            else:
+                by_pos = dict(zip(pos[g].tolist(), scores[g].tolist()))
+                ref = tr["kept_scores"]
+                got = np.array([by_pos[p] for p in tr["kept"].tolist()])
+                if len(ref):
+                    rel = np.max(np.abs(got - ref) / np.maximum(ref, 1e-30))
+                    rep.score_max_rel = max(rep.score_max_rel, float(rel))
+            if tr["margin"] < oracle.NEAR_TIE:
+                rep.near_ties += 1
+
+        dmax, dsum, dcnt = 0.0, 0.0, 0
+        qs = Qd[:, :, T:].permute(2, 0, 1, 3).contiguous()  # [S, B, H, d]
+        ks = Kd[:, :, T:].permute(2, 0, 1, 3).contiguous()
+        vs = Vd[:, :, T:].permute(2, 0, 1, 3).contiguous()
+        dout = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+        for s in range(S):
+            h2o.h2o_decode_step(ctx, 0, qs[s], ks[s], vs[s], dout)
+            ev = h2o.h2o_last_evicted(ctx, 0)
+            o = dout.reshape(B * H, d)[gpu_rows].cpu().numpy().astype(np.float64)
+            if copies is not None:  # every copy of a row must evict the same position
+                for i in range(len(rows)):
+                    same = ev[copies == i]
+                    if not np.all(same == same[0]):
+                        rep.mismatches.append((s, "copies", i, same.tolist(), None))
+            do_sets = set_check_every and ((s + 1) % set_check_every == 0 or s == S - 1)
+            pos = h2o.h2o_cache_positions(ctx, 0) if do_sets else None
+            scores = view["score"].cpu().numpy() if do_sets else None
+            for gi, (g, ti) in enumerate(check):
+                tr = traces[ti]
+                e = np.abs(o[gi] - tr["outs"][s])
+                dmax = max(dmax, float(e.max()))
+                dsum += float(e.sum())
+                dcnt += e.size
+                rep.evict_checks += 1
+                margin = tr["margins"][s]
+                near = margin < oracle.NEAR_TIE
+                rep.near_ties += int(near)
+                if ev[g] != tr["evicted"][s]:
+                    if near:
+                        rep.near_tie_mismatches += 1
+                        rep.resyncs += 1
+                        _, kb, vb = row_bits[ti]
+                        _resync_row(view, g, tr["kept_after"][s], tr["scores_after"][s], kb, vb, k,
+                                    T + s + 1)
+                        continue
+                    rep.mismatches.append((s, g, int(ev[g]), int(tr["evicted"][s]), margin))
+                    continue
+                if do_sets:
+                    gp = np.sort(pos[g][pos[g] >= 0])
+                    rep.set_checks += 1
+                    if not np.array_equal(gp, tr["kept_after"][s]):
+                        rep.mismatches.append((s, g, "set", gp.tolist(), tr["kept_after"][s].tolist()))
+                    else:
+                        by_pos = dict(zip(pos[g].tolist(), scores[g].tolist()))
+                        ref = tr["scores_after"][s]
+                        got = np.array([by_pos[p] for p in tr["kept_after"][s].tolist()])
+                        rel = np.max(np.abs(got - ref) / np.maximum(ref, 1e-30))
+                        rep.score_max_rel = max(rep.score_max_rel, float(rel))
+        if dcnt:
+            rep.decode_max_abs = dmax
+            rep.decode_mean_abs = dsum / dcnt
+        h2o.h2o_sync_check(ctx)
+    finally:
+        ctx.close()
+    return rep

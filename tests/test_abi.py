@@ -1,0 +1,56 @@
+"""The C-ABI library loads and exports every entry point include/*.h declares (CPU only).
+
+No compute call is made: the library is loaded and its symbols are resolved.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(h2o_\w+)\s*\(", src))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from h2o_heavy_hitter_gb300 import _build
+    path = _build.build()
+    return ctypes.CDLL(str(path))
+
+
+def test_header_declares_entry_points():
+    names = _declared()
+    for n in ("h2o_create", "h2o_prefill", "h2o_decode_step", "h2o_cache_positions",
+              "h2o_destroy", "h2o_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_last_error_is_callable_without_gpu(lib):
+    lib.h2o_last_error.restype = ctypes.c_char_p
+    assert lib.h2o_last_error() == b""
+
+
+def test_null_context_calls_fail_cleanly_without_gpu(lib):
+    """Argument checks run before any CUDA call."""
+    lib.h2o_cache_dims.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert lib.h2o_cache_dims(None, None, None) == -1
+    lib.h2o_create.argtypes = [ctypes.c_int] * 6 + [ctypes.c_void_p]
+    out = ctypes.c_void_p()
+    assert lib.h2o_create(1, 1, 1, 96, 1, 1, ctypes.byref(out)) == -1
+    assert out.value is None

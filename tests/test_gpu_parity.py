@@ -1,0 +1,148 @@
+"""GPU parity of the CUDA path (called through the C ABI) against the CPU oracle.
+
+Tolerances: outputs within 2e-2 max-abs and 2e-3 mean-abs of the fp64 oracle
+(bf16 inputs, fp32 accumulation); retained sets and evicted positions equal at
+every step whose oracle margin is at least 1e-4 (near-ties are counted and the
+GPU row is resynchronised to the oracle).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from h2o_parity import MAX_ABS, MEAN_ABS, run_parity
+from workloads import WORKLOADS, Workload, bf16_bits_to_f64, head_direction, row_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+def _h2o():
+    import h2o_heavy_hitter_gb300 as h2o
+    return h2o
+
+
+def _assert_ok(rep, label):
+    print(f"\n[{label}] rows={rep.rows} steps={rep.steps} evict_checks={rep.evict_checks} "
+          f"set_checks={rep.set_checks} near_ties={rep.near_ties} "
+          f"near_tie_mismatches={rep.near_tie_mismatches} "
+          f"prefill max/mean={rep.prefill_max_abs:.2e}/{rep.prefill_mean_abs:.2e} "
+          f"decode max/mean={rep.decode_max_abs:.2e}/{rep.decode_mean_abs:.2e} "
+          f"score max rel={rep.score_max_rel:.2e}")
+    assert not rep.mismatches, rep.mismatches[:5]
+    assert rep.prefill_max_abs <= MAX_ABS and rep.prefill_mean_abs <= MEAN_ABS
+    assert rep.decode_max_abs <= MAX_ABS and rep.decode_mean_abs <= MEAN_ABS
+
+
+def test_tiny_workload_every_row():
+    _assert_ok(run_parity(WORKLOADS["tiny"]), "tiny")
+
+
+# Small shapes spanning several 128-token tiles with a ragged tail, both head
+# dims, and the degenerate budgets.
+EDGE = [
+    # (name, batch, heads, d, T, S, h, r)
+    ("ragged-d128", 2, 3, 128, 300, 40, 40, 24),
+    ("ragged-d64", 2, 2, 64, 259, 33, 17, 9),
+    ("prompt-shorter-than-budget", 1, 3, 128, 50, 40, 40, 30),
+    ("prompt-equals-budget", 1, 2, 64, 64, 10, 32, 32),
+    ("heavy-only-r0", 1, 2, 128, 200, 30, 24, 0),
+    ("recent-only-h0", 1, 2, 128, 200, 30, 0, 24),
+    ("budget-one-recent", 1, 2, 64, 40, 12, 0, 1),
+    ("budget-one-heavy", 1, 2, 64, 40, 12, 1, 0),
+    ("single-token-prompt", 1, 2, 128, 1, 20, 4, 4),
+    ("large-budget-split", 1, 2, 128, 1500, 20, 300, 300),
+]
+
+
+@pytest.mark.parametrize("name,B,H,d,T,S,h,r", EDGE, ids=[e[0] for e in EDGE])
+def test_edge_shapes(name, B, H, d, T, S, h, r):
+    w = Workload(200 + EDGE.index((name, B, H, d, T, S, h, r)), name, 1, B, H, d, T, S, h, r, 0.8)
+    _assert_ok(run_parity(w), name)
+
+
+def test_empty_prompt_then_decode():
+    """T = 0: the cache starts empty and decode appends until it is full."""
+    w = Workload(250, "empty-prompt", 1, 1, 2, 64, 0, 30, 6, 4, 0.8)
+    _assert_ok(run_parity(w), "empty-prompt")
+
+
+def test_opt_6_7b_layer_every_row():
+    _assert_ok(run_parity(WORKLOADS["opt-6.7b-layer"], set_check_every=16), "opt-6.7b-layer")
+
+
+def test_prefill_attention_scores_match_oracle():
+    """Cache-free entry point: every row's output and column-sum scores."""
+    h2o = _h2o()
+    w = Workload(260, "attn", 1, 2, 3, 128, 333, 0, 8, 8, 0.8)
+    rows = [(b, j) for b in range(w.batch) for j in range(w.heads)]
+    bits = [row_tokens(w, 0, b, j, head_direction(w, 0, j)) for b, j in rows]
+    dev = torch.device("cuda")
+    to = lambda i: torch.from_numpy(np.stack([x[i] for x in bits]).view(np.int16)).to(dev).view(
+        torch.bfloat16)
+    out, score = h2o.h2o_prefill_attention(to(0), to(1), to(2))
+    out, score = out.cpu().numpy(), score.cpu().numpy()
+    for i, x in enumerate(bits):
+        q, k, v = (bf16_bits_to_f64(y) for y in x)
+        O, colsum, _ = oracle.prefill_attention(q, k, v, oracle.default_scale(w.head_dim))
+        assert np.abs(out[i] - O).max() <= MAX_ABS
+        assert np.abs(out[i] - O).mean() <= MEAN_ABS
+        np.testing.assert_allclose(score[i], colsum, rtol=2e-5, atol=1e-6)
+
+
+def test_decode_graph_replay_matches_eager():
+    """Decode steps captured in a CUDA graph replay like eager calls (device-side
+    step counter and fill count)."""
+    h2o = _h2o()
+    w = Workload(270, "graph", 1, 2, 4, 128, 180, 24, 20, 12, 0.8)
+    dev = torch.device("cuda")
+    rows = [(b, j) for b in range(w.batch) for j in range(w.heads)]
+    bits = [row_tokens(w, 0, b, j, head_direction(w, 0, j)) for b, j in rows]
+    full = [torch.from_numpy(np.stack([x[i] for x in bits]).view(np.int16)).to(dev).view(
+        torch.bfloat16).reshape(w.batch, w.heads, w.tokens, w.head_dim) for i in range(3)]
+    T, S = w.prompt, w.steps
+    pre = [x[:, :, :T].contiguous() for x in full]
+    step = [x[:, :, T:].permute(2, 0, 1, 3).contiguous() for x in full]
+    outs = []
+    for mode in ("eager", "graph"):
+        ctx = h2o.h2o_create(1, w.batch, w.heads, w.head_dim, w.h, w.r)
+        h2o.h2o_prefill(ctx, 0, *pre)
+        o = torch.zeros((S, w.batch, w.heads, w.head_dim), dtype=torch.float32, device=dev)
+        if mode == "eager":
+            for s in range(S):
+                h2o.h2o_decode_step(ctx, 0, step[0][s], step[1][s], step[2][s], o[s])
+        else:
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    for s in range(S):
+                        h2o.h2o_decode_step(ctx, 0, step[0][s], step[1][s], step[2][s], o[s])
+            torch.cuda.current_stream().wait_stream(side)
+            g.replay()
+        torch.cuda.synchronize()
+        outs.append((o.cpu(), h2o.h2o_cache_positions(ctx, 0)))
+        ctx.close()
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert np.array_equal(outs[0][1], outs[1][1])
+
+
+def test_error_codes():
+    h2o = _h2o()
+    with pytest.raises(h2o.H2OError) as e:
+        h2o.h2o_create(1, 1, 1, 96, 4, 4)
+    assert e.value.code == h2o.H2O_EINVAL
+    with pytest.raises(h2o.H2OError) as e:
+        h2o.h2o_create(1, 1, 1, 64, 0, 0)
+    assert e.value.code == h2o.H2O_EINVAL
+    ctx = h2o.h2o_create(2, 1, 2, 64, 4, 4)
+    x = torch.zeros((1, 2, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(h2o.H2OError) as e:
+        h2o.h2o_decode_step(ctx, 0, x, x, x)
+    assert e.value.code == h2o.H2O_ESTATE
+    with pytest.raises(h2o.H2OError) as e:
+        h2o.h2o_cache_positions(ctx, 2)
+    assert e.value.code == h2o.H2O_EINVAL
+    h2o.h2o_sync_check(ctx)
+    ctx.close()
