@@ -174,6 +174,22 @@ def _dist_env():
     return ws, rank, local
 
 
+def rank_layer_seed(rank: int) -> int:
+    """Layer index used to seed a rank's inputs: every rank draws an independent batch."""
+    return rank
+
+
+def max_over_ranks(value: float, pg, device=None) -> float:
+    """Maximum of a per-rank value over all ranks (identity without a process group)."""
+    if pg is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
 # --------------------------------------------------------------------------- reference arm
 def run_reference(args, w):
     ws, rank, _ = _dist_env()
@@ -239,10 +255,11 @@ def run_ours(args, w):
     # Inputs: each rank draws its own layer seed (independent batches).
     t0 = time.perf_counter()
     bits = np.empty((3, B, H, N, d), dtype=np.uint16)
-    dirs = [head_direction(w, rank, j) for j in range(H)]
+    seed_layer = rank_layer_seed(rank)
+    dirs = [head_direction(w, seed_layer, j) for j in range(H)]
     for b in range(B):
         for j in range(H):
-            q, k, v = row_tokens(w, rank, b, j, dirs[j])
+            q, k, v = row_tokens(w, seed_layer, b, j, dirs[j])
             bits[0, b, j], bits[1, b, j], bits[2, b, j] = q, k, v
     gen_s = time.perf_counter() - t0
 
@@ -304,11 +321,7 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     clk = clocks.stop()
     barrier()
-    elapsed_ms = start.elapsed_time(end)
-    if pg is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), pg, dev)
     prefill_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     decode_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
 
@@ -337,13 +350,11 @@ def run_ours(args, w):
             e2e_step()
         e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if pg is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), pg, dev)
 
-    # ---- decode launches with L2 flushed before each (HBM-cold reference point)
+    # ---- decode launches with L2 flushed before each (HBM-cold reference point).
+    # The flush writes a buffer twice the size of L2 and then reads it back, so
+    # L2 holds clean lines: the timed kernel pays no write-back of dirty data.
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     ctx_l2 = h2o.h2o_create(1, B, H, d, w.h, w.r)
     with torch.cuda.stream(stream):
@@ -353,6 +364,7 @@ def run_ours(args, w):
     with torch.cuda.stream(stream):
         for s in range(n_cold):
             flush.fill_(s & 0xff)
+            flush.sum(dtype=torch.int64)
             a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             h2o.h2o_decode_step(ctx_l2, 0, ds[0][s], ds[1][s], ds[2][s], dec_out[s])

@@ -61,14 +61,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete. Gives up after
-// kWaitLimitNs, OR-ing kErrWaitTimeout into *err and returning false.
+// kWaitLimitNs, OR-ing kErrWaitTimeout into *err (if err is not null) and
+// returning false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(err, kErrWaitTimeout);
+      if (err) atomicOr(err, kErrWaitTimeout);
       return false;
     }
   }

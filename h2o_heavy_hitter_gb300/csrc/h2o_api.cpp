@@ -64,6 +64,9 @@ struct h2o_ctx {
   float* score = nullptr;
   int32_t* pos = nullptr;
   int32_t* meta = nullptr;
+  float* logits = nullptr;    // decode scratch, per layer [rows][k]
+  float* partial = nullptr;   // decode scratch, per layer [rows][segs][d + 4]
+  int32_t* counter = nullptr; // decode scratch, per layer [rows], zero between steps
   int32_t* err = nullptr;     // device error word
   std::vector<int> prompt_len;  // per layer: -1 until prefilled
   h2o::DecodeConfig dcfg{};
@@ -73,6 +76,11 @@ struct h2o_ctx {
   float* layer_score(int l) const { return score + static_cast<size_t>(l) * rows * k; }
   int32_t* layer_pos(int l) const { return pos + static_cast<size_t>(l) * rows * k; }
   int32_t* layer_meta(int l) const { return meta + static_cast<size_t>(l) * rows * 4; }
+  float* layer_logits(int l) const { return logits + static_cast<size_t>(l) * rows * k; }
+  float* layer_partial(int l) const {
+    return partial + static_cast<size_t>(l) * rows * dcfg.segs * (d + 4);
+  }
+  int32_t* layer_counter(int l) const { return counter + static_cast<size_t>(l) * rows; }
 };
 
 namespace {
@@ -87,7 +95,7 @@ int check_layer(const h2o_ctx* c, int layer) {
 
 int run_attention(const void* Q, const void* K, const void* V, int rows, int T, int d, float* out,
                   float* colsum, int32_t* err, cudaStream_t s) {
-  Scratch lse(static_cast<size_t>(rows) * T * sizeof(float), s);
+  Scratch lse(static_cast<size_t>(rows) * h2o::lse_stride(T) * sizeof(float), s);
   cudaError_t e = h2o::prefill_forward(Q, K, V, rows, T, d, out, static_cast<float*>(lse.p), err, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefill forward launch");
   e = h2o::prefill_colsum(Q, K, static_cast<float*>(lse.p), rows, T, d, colsum, err, s);
@@ -134,12 +142,18 @@ int h2o_create(int layers, int batch, int heads, int head_dim, int h, int r, h2o
     return cuda_fail(e, "cudaDeviceGetAttribute");
   }
 
+  h2o::DecodeTuning tune{env_int("H2O_DECODE_THREADS"), env_int("H2O_DECODE_UNROLL"),
+                         env_int("H2O_DECODE_SEGS"), env_int("H2O_DECODE_PDL")};
+  c->dcfg = h2o::decode_config(c->rows, c->k, c->d, sms, tune);
+
   const size_t L = layers, R = c->rows, K = c->k, D = head_dim;
   c->kv_elems_per_layer = R * K * D;
   const size_t kv_bytes = align_up(L * R * K * D * 2, 256);
   const size_t sc_bytes = align_up(L * R * K * 4, 256);
   const size_t meta_bytes = align_up(L * R * 16, 256);
-  const size_t total = 2 * kv_bytes + 2 * sc_bytes + meta_bytes + 256;
+  const size_t part_bytes = align_up(L * R * c->dcfg.segs * (D + 4) * 4, 256);
+  const size_t cnt_bytes = align_up(L * R * 4, 256);
+  const size_t total = 2 * kv_bytes + 3 * sc_bytes + meta_bytes + part_bytes + cnt_bytes + 256;
   cudaStream_t s = current_stream();
   try {
     c->base = c10::cuda::CUDACachingAllocator::raw_alloc_with_stream(total, s);
@@ -156,24 +170,24 @@ int h2o_create(int layers, int batch, int heads, int head_dim, int h, int r, h2o
   p += sc_bytes;
   c->pos = reinterpret_cast<int32_t*>(p);
   p += sc_bytes;
+  c->logits = reinterpret_cast<float*>(p);
+  p += sc_bytes;
   c->meta = reinterpret_cast<int32_t*>(p);
   p += meta_bytes;
+  c->partial = reinterpret_cast<float*>(p);
+  p += part_bytes;
+  c->counter = reinterpret_cast<int32_t*>(p);
+  p += cnt_bytes;
   c->err = reinterpret_cast<int32_t*>(p);
 
   e = cudaMemsetAsync(c->err, 0, sizeof(int32_t), s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->K, 0, 2 * kv_bytes, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->counter, 0, cnt_bytes, s);
   for (int l = 0; l < layers && e == cudaSuccess; ++l)
     e = h2o::cache_reset(c->rows, c->k, c->layer_score(l), c->layer_pos(l), c->layer_meta(l), s);
   if (e != cudaSuccess) {
     h2o_destroy(c);
     return cuda_fail(e, "cache initialisation");
-  }
-  c->dcfg = h2o::decode_config(c->rows, c->k, c->d, sms, env_int("H2O_DECODE_CLUSTER"),
-                               env_int("H2O_DECODE_STAGES"));
-  e = h2o::decode_prepare(c->dcfg, c->d);
-  if (e != cudaSuccess) {
-    h2o_destroy(c);
-    return cuda_fail(e, "decode kernel attributes");
   }
   *out = c;
   return H2O_OK;
@@ -243,14 +257,17 @@ int h2o_decode_step(h2o_ctx* c, int layer, const void* q, const void* k_new, con
   a.score = c->layer_score(layer);
   a.pos = c->layer_pos(layer);
   a.meta = c->layer_meta(layer);
+  a.logits = c->layer_logits(layer);
+  a.partial = c->layer_partial(layer);
+  a.counter = c->layer_counter(layer);
   a.q = q;
   a.k_new = k_new;
   a.v_new = v_new;
   a.out = out;
-  a.err = c->err;
   a.k = c->k;
   a.r = c->r;
-  a.chunk = c->dcfg.chunk;
+  a.segs = c->dcfg.segs;
+  a.seg_len = c->dcfg.seg_len;
   a.qscale = h2o::kLog2e / std::sqrt(static_cast<float>(c->d));
   cudaError_t e = h2o::decode_launch(a, c->dcfg, c->rows, c->d, current_stream());
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");

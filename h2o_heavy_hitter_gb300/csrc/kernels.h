@@ -11,42 +11,55 @@ namespace h2o {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---- decode ------------------------------------------------------------------
+constexpr int kMaxDecodeSegs = 64;  // most CTAs one row's decode step is split over
+
 struct DecodeArgs {
   void* Kc;           // bf16 [rows][k][d] cached keys of one layer
   void* Vc;           // bf16 [rows][k][d] cached values
   float* score;       // [rows][k] accumulated scores
   int32_t* pos;       // [rows][k] positions (-1 empty)
   int32_t* meta;      // [rows][4] {filled, next position, last evicted, 0}
+  float* logits;      // [rows][k] scratch: this step's base-2 logits
+  float* partial;     // [rows][segs][d + 4] scratch: {max, sum, -, -, output[d]} per segment
+  int32_t* counter;   // [rows] scratch: segments arrived this step (0 between steps)
   const void* q;      // bf16 [rows][d]
   const void* k_new;  // bf16 [rows][d]
   const void* v_new;  // bf16 [rows][d]
   float* out;         // [rows][d]
-  int32_t* err;       // device error word
   int k;              // slots per row (h + r)
   int r;              // recent window
-  int chunk;          // slots handled by one CTA of a row's cluster
+  int segs;           // CTAs per row
+  int seg_len;        // slots per segment (the last may be shorter)
   float qscale;       // log2(e) / sqrt(d)
 };
 
+// Launch shape of the decode kernel. Zero / out-of-range values pick defaults.
+struct DecodeTuning {
+  int threads;  // 128 or 256 threads per CTA
+  int unroll;   // slots per group per batch (2 or 4)
+  int segs;     // CTAs per row; 0 = automatic
+  int pdl;      // < 0: launch without programmatic dependent launch
+};
+
 struct DecodeConfig {
-  int cluster;  // CTAs per row (1, 2, 4, 8 or 16)
-  int chunk;    // ceil(k / cluster)
-  int stages;   // bulk-copy stages in flight per CTA
-  size_t smem;  // dynamic shared memory per CTA
+  bool pdl;     // programmatic dependent launch (overlaps the previous kernel's tail)
+  int threads, unroll;
+  int segs;     // CTAs per row
+  int seg_len;  // slots per segment
 };
 
 // Picks the launch shape for (rows, k, d) on a device with `num_sms` SMs.
-// `cluster_override` / `stages_override` > 0 force a value.
-DecodeConfig decode_config(int rows, int k, int d, int num_sms, int cluster_override,
-                           int stages_override);
-// Sets the kernel attributes a configuration needs (call once, outside capture).
-cudaError_t decode_prepare(const DecodeConfig& cfg, int d);
+DecodeConfig decode_config(int rows, int k, int d, int num_sms, const DecodeTuning& tune);
 cudaError_t decode_launch(const DecodeArgs& a, const DecodeConfig& cfg, int rows, int d,
                           cudaStream_t stream);
 
 // ---- prefill -----------------------------------------------------------------
+// Row stride (floats) of the per-row log-sum-exp scratch: T rounded up to a
+// whole 128-token tile, so every tile's slice is 512-byte aligned.
+inline int lse_stride(int T) { return (T + 127) / 128 * 128; }
+
 // Causal attention over `rows` rows of T tokens: O (fp32 [rows][T][d]) and the
-// base-2 log-sum-exp of each query row's scaled logits (fp32 [rows][T]).
+// base-2 log-sum-exp of each query row's scaled logits (fp32 [rows][lse_stride(T)]).
 cudaError_t prefill_forward(const void* Q, const void* K, const void* V, int rows, int T, int d,
                             float* O, float* lse2, int32_t* err, cudaStream_t stream);
 // Column sums of the causal probability matrix (fp32 [rows][T]), given lse2.

@@ -92,20 +92,27 @@ def _to_bf16(bits: np.ndarray, device) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
 
 
-def _resync_row(view, gpu_row: int, pos: np.ndarray, scores: np.ndarray, k_bits, v_bits, k: int,
+def _resync_row(view, gpu_rows, pos: np.ndarray, scores: np.ndarray, k_bits, v_bits, k: int,
                 t_next: int):
-    """Overwrite one GPU row with the oracle's retained set (slot order = ascending position)."""
+    """Overwrite GPU rows (every copy of one checked row) with the oracle's
+    retained set, slots in ascending position order."""
     n = len(pos)
     dev = view["pos"].device
+    rows_t = torch.as_tensor(np.atleast_1d(gpu_rows), device=dev, dtype=torch.long)
     pos_full = np.full(k, -1, dtype=np.int32)
     pos_full[:n] = pos
     sc_full = np.zeros(k, dtype=np.float32)
     sc_full[:n] = scores
-    view["pos"][gpu_row] = torch.from_numpy(pos_full).to(dev)
-    view["score"][gpu_row] = torch.from_numpy(sc_full).to(dev)
-    view["K"][gpu_row, :n] = _to_bf16(k_bits[pos], dev)
-    view["V"][gpu_row, :n] = _to_bf16(v_bits[pos], dev)
-    view["meta"][gpu_row] = torch.tensor([n, t_next, -1, 0], dtype=torch.int32, device=dev)
+    view["pos"][rows_t] = torch.from_numpy(pos_full).to(dev)
+    view["score"][rows_t] = torch.from_numpy(sc_full).to(dev)
+    kk = torch.zeros((k, k_bits.shape[1]), dtype=torch.bfloat16, device=dev)
+    vv = torch.zeros_like(kk)
+    if n:
+        kk[:n] = _to_bf16(k_bits[pos], dev)
+        vv[:n] = _to_bf16(v_bits[pos], dev)
+    view["K"][rows_t] = kk
+    view["V"][rows_t] = vv
+    view["meta"][rows_t] = torch.tensor([n, t_next, -1, 0], dtype=torch.int32, device=dev)
 
 
 def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool = False,
@@ -128,13 +135,13 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
     row_bits = [row_tokens(w, layer, b, j, head_direction(w, layer, j)) for (b, j) in rows]
     if tile:
         src = [i % len(rows) for i in range(B * H)]
-        gpu_of = {}  # checked gpu row -> trace index (first copy)
-        for g, s in enumerate(src):
-            gpu_of.setdefault(s, g)
+        gpu_of = {}  # trace index -> first gpu row holding a copy of it
+        for g, s_ in enumerate(src):
+            gpu_of.setdefault(s_, g)
         check = [(gpu_of[i], i) for i in range(len(rows))]
-        allq = np.stack([row_bits[s][0] for s in src]).reshape(B, H, N, d)
-        allk = np.stack([row_bits[s][1] for s in src]).reshape(B, H, N, d)
-        allv = np.stack([row_bits[s][2] for s in src]).reshape(B, H, N, d)
+        idx = torch.tensor(src, device=dev)
+        Qd, Kd, Vd = (_to_bf16(np.stack([x[c] for x in row_bits]), dev)[idx].reshape(B, H, N, d)
+                      for c in range(3))
         copies = np.array(src)
     else:
         from workloads import layer_tokens
@@ -146,7 +153,10 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
             allq, allk, allv = layer_tokens(w, layer)
         check = [(b * H + j, i) for i, (b, j) in enumerate(rows)]
         copies = None
-    Qd, Kd, Vd = (_to_bf16(x, dev) for x in (allq, allk, allv))
+        Qd, Kd, Vd = (_to_bf16(x, dev) for x in (allq, allk, allv))
+
+    def copies_of(g, ti):
+        return np.nonzero(copies == ti)[0] if copies is not None else [g]
 
     rep = Report(rows=len(check), steps=S)
     ctx = h2o.h2o_create(1, B, H, d, w.h, w.r)
@@ -171,9 +181,8 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
                 if tr["margin"] < oracle.NEAR_TIE:
                     rep.near_tie_mismatches += 1
                     rep.resyncs += 1
-                    b_, j_ = rows[ti]
                     _, kb, vb = row_bits[ti]
-                    _resync_row(view, g, tr["kept"], tr["kept_scores"], kb, vb, k, T)
+                    _resync_row(view, copies_of(g, ti), tr["kept"], tr["kept_scores"], kb, vb, k, T)
                 else:
                     rep.mismatches.append((-1, g, gp.tolist(), tr["kept"].tolist(), tr["margin"]))
             else:
@@ -218,8 +227,8 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
                         rep.near_tie_mismatches += 1
                         rep.resyncs += 1
                         _, kb, vb = row_bits[ti]
-                        _resync_row(view, g, tr["kept_after"][s], tr["scores_after"][s], kb, vb, k,
-                                    T + s + 1)
+                        _resync_row(view, copies_of(g, ti), tr["kept_after"][s], tr["scores_after"][s],
+                                    kb, vb, k, T + s + 1)
                         continue
                     rep.mismatches.append((s, g, int(ev[g]), int(tr["evicted"][s]), margin))
                     continue
