@@ -246,6 +246,28 @@ int h2o_prefill_attention(const void* Q, const void* K, const void* V, int rows,
   }
 }
 
+int h2o_prefill_attention_noalloc(const void* Q, const void* K, const void* V, int rows, int T,
+                                  int head_dim, float* out, float* score, void* stream) {
+  if (rows < 0 || T < 0 || T > H2O_MAX_T) return fail(H2O_EINVAL, "rows or T out of range");
+  if (head_dim != 64 && head_dim != 128) return fail(H2O_EINVAL, "head_dim must be 64 or 128");
+  const long need = static_cast<long>(rows) * h2o::lse_stride(T);
+  if (need > H2O_NOALLOC_MAX_LSE)
+    return fail(H2O_EINVAL, "rows * ceil(T / 128) * 128 = " + std::to_string(need) +
+                                " exceeds the fixed scratch of H2O_NOALLOC_MAX_LSE = " +
+                                std::to_string(H2O_NOALLOC_MAX_LSE) + " floats");
+  if (need == 0) return H2O_OK;
+  if (!Q || !K || !V || !out || !score) return fail(H2O_EINVAL, "null pointer");
+  float* lse = nullptr;
+  cudaError_t e = h2o::noalloc_lse_scratch(&lse);
+  if (e != cudaSuccess) return cuda_fail(e, "scratch address lookup");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  e = h2o::prefill_forward(Q, K, V, rows, T, head_dim, out, lse, nullptr, s);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill forward launch");
+  e = h2o::prefill_colsum(Q, K, lse, rows, T, head_dim, score, nullptr, s);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill column-sum launch");
+  return H2O_OK;
+}
+
 int h2o_decode_step(h2o_ctx* c, int layer, const void* q, const void* k_new, const void* v_new,
                     float* out) {
   if (int rc = check_layer(c, layer)) return rc;

@@ -65,6 +65,11 @@ cudaError_t prefill_forward(const void* Q, const void* K, const void* V, int row
 // Column sums of the causal probability matrix (fp32 [rows][T]), given lse2.
 cudaError_t prefill_colsum(const void* Q, const void* K, const float* lse2, int rows, int T,
                            int d, float* colsum, int32_t* err, cudaStream_t stream);
+// Device address of the library's fixed log-sum-exp array used by
+// h2o_prefill_attention_noalloc (H2O_NOALLOC_MAX_LSE floats). Looked up once
+// per device, with that device current, and cached.
+cudaError_t noalloc_lse_scratch(float** out);
+
 // Top-h plus recent selection of every row into the cache's pos/score/meta.
 cudaError_t prefill_select(const float* colsum, int rows, int T, int h, int r, float* score,
                            int32_t* pos, int32_t* meta, cudaStream_t stream);

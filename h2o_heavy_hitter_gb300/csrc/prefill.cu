@@ -27,8 +27,10 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
+#include "h2o.h"
 #include "kernels.h"
 #include "tc.cuh"
 
@@ -614,6 +616,35 @@ cudaError_t prefill_colsum(const void* Q, const void* K, const float* lse2, int 
   if (static_cast<long>(rows) * T == 0) return cudaSuccess;
   return d == 128 ? colsum_t<128>(Q, K, lse2, rows, T, colsum, err, stream)
                   : colsum_t<64>(Q, K, lse2, rows, T, colsum, err, stream);
+}
+
+// ------------------------------------------------------------------ allocation-free scratch
+// Per-row log-sum-exp for h2o_prefill_attention_noalloc lives in this fixed
+// file-scope device array instead of an allocation. Host code must not pass
+// the symbol itself to a kernel (on the host it is only a stand-in); its
+// device address is looked up per device below.
+static __device__ __align__(256) float g_noalloc_lse[H2O_NOALLOC_MAX_LSE];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+float* g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+cudaError_t noalloc_lse_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_lse);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace h2o

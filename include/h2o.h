@@ -133,6 +133,42 @@ int h2o_prefill_attention(const void* Q, const void* K, const void* V, int rows,
                           int head_dim, float* out, float* score);
 
 /*
+ * h2o_prefill_attention_noalloc - the same computation as h2o_prefill_attention
+ * (outputs and column-sum scores of `rows` cache-free rows), for callers that
+ * must not allocate device memory during the call. The pages have no
+ * counterpart to this entry point; it exists for the caller, not the policy.
+ *
+ * Who needs it: callers for which a device allocation during the call is not
+ * an option. A serving process may reserve its device memory once at start-up
+ * and forbid allocation on the request path, because cudaMalloc can block
+ * until the device is idle and stall every stream. A process whose memory is
+ * pre-reserved by another framework's arena (one that grabs most of the GPU up
+ * front) has little free memory left, so an extra allocation can fail there.
+ * Such callers cannot use h2o_prefill_attention, whose per-row log-sum-exp
+ * scratch comes from PyTorch's caching allocator.
+ *
+ * Instead the scratch is a fixed device array inside the library
+ * (H2O_NOALLOC_MAX_LSE floats, 4 MiB, held by every GPU that loads the
+ * library until the process exits). This call allocates nothing, uses no
+ * PyTorch state and enqueues its kernels on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream). The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture. All calls share the one array, so
+ * calls whose work overlaps on the GPU (different streams, or different
+ * threads without ordering between them) race on it; calls on one stream are
+ * ordered and safe. Nothing in the array needs to start at zero: every entry a
+ * call reads was written earlier by the same call.
+ *
+ * Q, K, V: device bf16 [rows, T, d]; out: device fp32 [rows, T, d];
+ * score: device fp32 [rows, T]. Limit: rows * (T rounded up to a multiple of
+ * 128) <= H2O_NOALLOC_MAX_LSE; larger calls are rejected with H2O_EINVAL and
+ * a message. Errors: H2O_EINVAL, H2O_ECUDA.
+ */
+#define H2O_NOALLOC_MAX_LSE (1 << 20)
+int h2o_prefill_attention_noalloc(const void* Q, const void* K, const void* V, int rows, int T,
+                                  int head_dim, float* out, float* score, void* stream);
+
+/*
  * h2o_cache_positions - copy the positions held by every slot of one layer to
  * host memory: host_pos int32 [batch * heads * k], row-major by (row, slot),
  * -1 for empty slots. Synchronises the current stream.
