@@ -30,6 +30,8 @@ namespace h2o {
 namespace {
 
 constexpr int kNewSlot = -2;  // argmin slot value meaning "the new token itself"
+constexpr int kSoloSlots = 8192;  // longest row whose logits stay in shared memory
+constexpr int kSoloRegs = 4;      // slots per thread whose score/position is preloaded
 
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -83,7 +85,8 @@ struct DecodeShared {
   int target;
 };
 
-template <int D, int NT, int U>
+// PIPE: two batches of U slots per group in flight (software pipelining).
+template <int D, int NT, int U, bool PIPE>
 __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   using Sm = DecodeShared<D, NT>;
   constexpr int LPS = Sm::LPS, G = Sm::G, NW = Sm::NW;
@@ -133,17 +136,37 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   for (int i = 0; i < 8; ++i) o[i] = 0.f;
   const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(a.Kc) + (rk + s0) * D + l * 8;
   const __nv_bfloat16* Vg = static_cast<const __nv_bfloat16*>(a.Vc) + (rk + s0) * D + l * 8;
-  float* lg_out = a.logits + rk + s0;
-  for (int base = g; base < cap; base += G * U) {
-    uint4 kv[U], vv[U];
+  // A row handled by a single CTA keeps its logits in shared memory; split rows
+  // hand them to the finishing CTA through the per-layer scratch.
+  extern __shared__ float solo_logits[];
+  const bool solo = a.segs == 1 && a.k <= kSoloSlots;
+  float* lg_out = solo ? solo_logits : a.logits + rk + s0;
+  // Single-CTA rows: this thread's slots' scores and positions, loaded now so
+  // that their latency hides behind the K/V sweep.
+  const int filled = min(count, a.k);
+  float sc_r[kSoloRegs];
+  int ps_r[kSoloRegs];
+#pragma unroll
+  for (int jj = 0; jj < kSoloRegs; ++jj) {
+    const int i = tid + jj * NT;
+    if (solo && i < filled) {
+      sc_r[jj] = a.score[rk + i];
+      ps_r[jj] = a.pos[rk + i];
+    }
+  }
+  // One batch: U slots of this group, loaded by capacity (slots past the fill
+  // count are masked when consumed).
+  auto load = [&](uint4 (&kv)[U], uint4 (&vv)[U], int base) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int i = base + u * G;
-      if (i < cap) {  // load by capacity; slots past the fill count are masked below
+      if (i < cap) {
         kv[u] = ldg_stream(Kg + static_cast<size_t>(i) * D);
         vv[u] = ldg_stream(Vg + static_cast<size_t>(i) * D);
       }
     }
+  };
+  auto consume = [&](const uint4 (&kv)[U], const uint4 (&vv)[U], int base) {
     float s[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) s[u] = dot8(kv[u], qf);
@@ -169,6 +192,26 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
         accum8(o, p, vv[u]);
         if (l == 0) lg_out[i] = s[u];
       }
+    }
+  };
+  constexpr int STEP = G * U;
+  if constexpr (PIPE) {
+    // Two batches in flight: the next batch's loads are issued before the
+    // current batch is consumed, so memory is never idle between batches.
+    uint4 ka[U], va[U], kb[U], vb[U];
+    if (g < cap) load(ka, va, g);
+    for (int base = g; base < cap; base += 2 * STEP) {
+      if (base + STEP < cap) load(kb, vb, base + STEP);
+      consume(ka, va, base);
+      if (base + STEP >= cap) break;
+      if (base + 2 * STEP < cap) load(ka, va, base + 2 * STEP);
+      consume(kb, vb, base + STEP);
+    }
+  } else {
+    for (int base = g; base < cap; base += STEP) {
+      uint4 kv[U], vv[U];
+      load(kv, vv, base);
+      consume(kv, vv, base);
     }
   }
   grid_launch_dependents();
@@ -268,14 +311,27 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   }
 
   // Scores of every occupied slot of the row; this CTA's smallest candidate key.
-  const int filled = min(count, a.k);
   const int thr = t - a.r;  // candidates: positions <= t - r
   unsigned long long best = ~0ull;
   int bslot = -1;
-  for (int i = tid; i < filled; i += NT) {
-    const float ns = a.score[rk + i] + ex2(__ldcg(a.logits + rk + i) - M) * invL;
+#pragma unroll 1
+  for (int jj = 0, i = tid; i < filled; ++jj, i += NT) {
+    float sc;
+    int ps;
+    if (solo && jj < kSoloRegs) {
+#pragma unroll
+      for (int q = 0; q < kSoloRegs; ++q)  // register arrays need static indices
+        if (q == jj) {
+          sc = sc_r[q];
+          ps = ps_r[q];
+        }
+    } else {
+      sc = a.score[rk + i];
+      ps = a.pos[rk + i];
+    }
+    const float lg = solo ? solo_logits[i] : __ldcg(a.logits + rk + i);
+    const float ns = sc + ex2(lg - M) * invL;
     a.score[rk + i] = ns;
-    const int ps = a.pos[rk + i];
     if (ps <= thr) {
       const unsigned long long key = pack_key(ns, ps);
       if (key < best) {
@@ -344,13 +400,14 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
 using KernelFn = void (*)(DecodeArgs);
 
 template <int D, int NT>
-KernelFn pick_u(int unroll) {
-  return unroll == 2 ? decode_kernel<D, NT, 2> : decode_kernel<D, NT, 4>;
+KernelFn pick_u(const DecodeConfig& c) {
+  if (c.pipe) return c.unroll == 2 ? decode_kernel<D, NT, 2, true> : decode_kernel<D, NT, 4, true>;
+  return c.unroll == 2 ? decode_kernel<D, NT, 2, false> : decode_kernel<D, NT, 4, false>;
 }
 
 KernelFn pick(const DecodeConfig& c, int d) {
-  if (d == 128) return c.threads == 256 ? pick_u<128, 256>(c.unroll) : pick_u<128, 128>(c.unroll);
-  return c.threads == 256 ? pick_u<64, 256>(c.unroll) : pick_u<64, 128>(c.unroll);
+  if (d == 128) return c.threads == 256 ? pick_u<128, 256>(c) : pick_u<128, 128>(c);
+  return c.threads == 256 ? pick_u<64, 256>(c) : pick_u<64, 128>(c);
 }
 
 }  // namespace
@@ -359,11 +416,19 @@ DecodeConfig decode_config(int rows, int k, int d, int num_sms, const DecodeTuni
   DecodeConfig c{};
   c.unroll = tune.unroll == 2 || tune.unroll == 4 ? tune.unroll : 4;
   c.pdl = tune.pdl >= 0;
-  // With at least one row per SM, one 256-thread CTA per row finishes its own
-  // row (no partials). With fewer rows than SMs, rows are split into segments
-  // of 128-thread CTAs until the grid covers every SM about eight times.
+  // Measured on GB300 (decode sweeps over the workload shapes):
+  //  * many rows (>= 4 per SM): one 128-thread CTA per row, one batch in flight;
+  //  * one to four rows per SM: one 256-thread CTA per row with two batches in
+  //    flight per group (software pipelining), which keeps memory busy across
+  //    the serial batches of a long row;
+  //  * fewer rows than SMs: rows split into segments of 128-thread CTAs until
+  //    the grid covers every SM about eight times.
   const bool few_rows = rows < num_sms;
-  c.threads = tune.threads == 128 || tune.threads == 256 ? tune.threads : (few_rows ? 128 : 256);
+  const bool many_rows = rows >= 4 * num_sms;
+  c.threads = tune.threads == 128 || tune.threads == 256
+                  ? tune.threads
+                  : (few_rows || many_rows ? 128 : 256);
+  c.pipe = tune.pipe > 0 || (tune.pipe == 0 && !few_rows && !many_rows);
   const int groups = c.threads / (d / 8);
   int segs = 1;
   if (tune.segs > 0) {
@@ -377,6 +442,7 @@ DecodeConfig decode_config(int rows, int k, int d, int num_sms, const DecodeTuni
   if (segs > kMaxDecodeSegs) segs = kMaxDecodeSegs;
   c.seg_len = (k + segs - 1) / segs;
   c.segs = (k + c.seg_len - 1) / c.seg_len;  // no empty trailing segment
+  c.smem = c.segs == 1 && k <= kSoloSlots ? static_cast<size_t>(k) * sizeof(float) : 0;
   return c;
 }
 
@@ -386,7 +452,7 @@ cudaError_t decode_launch(const DecodeArgs& a, const DecodeConfig& cfg, int rows
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(static_cast<unsigned>(rows) * static_cast<unsigned>(cfg.segs));
   lc.blockDim = dim3(static_cast<unsigned>(cfg.threads));
-  lc.dynamicSmemBytes = 0;
+  lc.dynamicSmemBytes = cfg.smem;
   lc.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -143,7 +143,8 @@ int h2o_create(int layers, int batch, int heads, int head_dim, int h, int r, h2o
   }
 
   h2o::DecodeTuning tune{env_int("H2O_DECODE_THREADS"), env_int("H2O_DECODE_UNROLL"),
-                         env_int("H2O_DECODE_SEGS"), env_int("H2O_DECODE_PDL")};
+                         env_int("H2O_DECODE_SEGS"), env_int("H2O_DECODE_PDL"),
+                         env_int("H2O_DECODE_PIPE")};
   c->dcfg = h2o::decode_config(c->rows, c->k, c->d, sms, tune);
 
   const size_t L = layers, R = c->rows, K = c->k, D = head_dim;

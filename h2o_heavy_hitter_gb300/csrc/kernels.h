@@ -39,13 +39,16 @@ struct DecodeTuning {
   int unroll;   // slots per group per batch (2 or 4)
   int segs;     // CTAs per row; 0 = automatic
   int pdl;      // < 0: launch without programmatic dependent launch
+  int pipe;     // > 0: two batches per group in flight; < 0: one; 0: automatic
 };
 
 struct DecodeConfig {
   bool pdl;     // programmatic dependent launch (overlaps the previous kernel's tail)
+  bool pipe;    // two batches per group in flight
   int threads, unroll;
   int segs;     // CTAs per row
   int seg_len;  // slots per segment
+  size_t smem;  // dynamic shared memory per CTA (logits of a single-CTA row)
 };
 
 // Picks the launch shape for (rows, k, d) on a device with `num_sms` SMs.

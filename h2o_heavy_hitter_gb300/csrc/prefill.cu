@@ -39,7 +39,8 @@ namespace {
 
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per tile
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;        // 10 warps: TMA, MMA, 8 softmax
+constexpr int kSoftmaxThreads = 256;
 constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16
 
 template <int D>
@@ -51,7 +52,7 @@ struct FwdCfg {
   static constexpr uint32_t O_COL = 256;  // O: columns [256, 256 + D)
   static constexpr uint32_t P_COL = 384;  // two bf16 P buffers: columns [384, 448) and [448, 512)
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr size_t SMEM = static_cast<size_t>(1 + KST + VST) * TILE + 1024 + 1024;
+  static constexpr size_t SMEM = static_cast<size_t>(1 + KST + VST) * TILE + 1024 + 4096;
 };
 
 struct FwdBars {
@@ -62,13 +63,20 @@ struct FwdBars {
   uint64_t o_done;  // one phase per PV (waited only by the rare O rescale)
   uint64_t o_last;  // one phase per item: its last PV has completed
   uint64_t o_free;  // one phase per item: the epilogue has read O out of TMEM
+  uint64_t xbar[4];  // per lane quadrant, one phase per tile: both halves' maxima posted
+  uint64_t ebar[4];  // per lane quadrant, one phase per item: both halves' sums posted
+  float xmax[2][2][128];  // [tile parity][half][row]
+  float xsum[2][128];     // [half][row]
   uint32_t tmem;
 };
+
+static_assert(sizeof(FwdBars) <= 4096, "FwdBars must fit the space reserved in FwdCfg::SMEM");
 
 struct FwdParams {
   float* O;
   float* lse2;
   int rows, T, Tp, nqt, items;
+  int rb;  // rows per L2 block of the item order
   float qscale;
   int32_t* err;
 };
@@ -90,6 +98,22 @@ __device__ __forceinline__ void load_tile(void* dst, const CUtensorMap* map, int
 // tcgen05.ld / st divergently.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+}
+
+// Item order shared by both kernels. Rows are taken in blocks of `rb` rows
+// whose K/V (forward) or Q (column sums) fit comfortably in L2, so the several
+// tiles of a row that read the same operand tiles run close together in time;
+// inside a block, items with more tiles come first. Returns the row and the
+// tile rank (0 = the item with the most tiles).
+__device__ __forceinline__ void item_coords(int it, int rows, int nqt, int rb, int& row,
+                                            int& rank) {
+  const int per_block = rb * nqt;
+  const int b = it / per_block;
+  const int r0 = b * rb;
+  const int nb = min(rb, rows - r0);
+  const int w = it - b * per_block;
+  rank = w / nb;
+  row = r0 + w % nb;
 }
 
 // K-major operand (rows x D, D contiguous): k-step kk covers columns [16kk, 16kk + 16).
@@ -128,11 +152,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_ready[i], 128);
+      mbar_init(&bars->p_ready[i], kSoftmaxThreads);
     }
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->o_last, 1);
-    mbar_init(&bars->o_free, 128);
+    mbar_init(&bars->o_free, kSoftmaxThreads);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars->xbar[i], 2);
+      mbar_init(&bars->ebar[i], 2);
+    }
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -156,7 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int j = 0;
       for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x, ++j) {
-        const int qt = p.nqt - 1 - it / p.rows, row = it % p.rows;
+        int row, rank;
+        item_coords(it, p.rows, p.nqt, p.rb, row, rank);
+        const int qt = p.nqt - 1 - rank;
         if (j > 0 && !mbar_wait(&bars->q_empty, (j - 1) & 1, p.err)) break;  // last QK^T done
         mbar_arrive_expect_tx(&bars->q_full, C::TILE);
         load_tile<D>(sQ, &tq, qt, row, &bars->q_full);
@@ -186,7 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int j = 0;
       for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x, ++j) {
-        const int nkt = p.nqt - it / p.rows;
+        int row, rank;
+        item_coords(it, p.rows, p.nqt, p.rb, row, rank);
+        const int nkt = p.nqt - rank;
         if (!mbar_wait(&bars->q_full, j & 1, p.err)) break;
         for (int kt = 0; kt <= nkt; ++kt) {
           if (kt < nkt) {
@@ -234,15 +266,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------------------------------------------------------- softmax (one query row per thread)
-    const int quad = warp & 3;
+    // ---------------------------------------------------------------- softmax
+    // Two warps per TMEM lane quadrant, one per half of the 128 S columns; a
+    // thread owns one query row's half. The halves share the row's running max
+    // (tile maxima exchanged through shared memory every tile) and add their
+    // row sums at the end of the item.
+    const int sw = warp - 2;
+    const int quad = warp & 3, half = sw >> 2;
     const int r = quad * 32 + lane;
+    const int cb = half * 64;  // first S column of this half
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     uint32_t g = 0;
     bool ok = true;
     int j = 0;
     for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x, ++j) {
-      const int qt = p.nqt - 1 - it / p.rows, row = it % p.rows;
+      int row, rank;
+      item_coords(it, p.rows, p.nqt, p.rb, row, rank);
+      const int qt = p.nqt - 1 - rank;
       const int nkt = qt + 1, qrow = qt * BM + r;
       float m = -INFINITY, l = 0.f;
       for (int kt = 0; kt < nkt; ++kt) {
@@ -253,20 +293,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        uint32_t s[BN];
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c)
-          tmem_ld32(tmem + lane_off + C::S_COL + sb * 128 + c * 32, s + c * 32);
+        uint32_t s[64];
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * 128 + cb, s);
+        tmem_ld32(tmem + lane_off + C::S_COL + sb * 128 + cb + 32, s + 32);
         tmem_wait_ld();
         if (kt == qt) {  // diagonal tile: key c is visible to query r iff c <= r
 #pragma unroll
-          for (int c = 0; c < BN; ++c)
-            if (c > r) s[c] = __float_as_uint(-INFINITY);
+          for (int c = 0; c < 64; ++c)
+            if (cb + c > r) s[c] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
+        float mx8[8];
 #pragma unroll
-        for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
-        mx *= p.qscale;
+        for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(s[e]);
+#pragma unroll
+        for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(s[c]));
+        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        // exchange the half maxima of this row with the partner warp
+        bars->xmax[gs & 1][half][r] = mx;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->xbar[quad]);
+        if (!warp_wait(&bars->xbar[quad], gs & 1, p.err)) {
+          ok = false;
+          break;
+        }
+        mx = fmaxf(mx, bars->xmax[gs & 1][half ^ 1][r]) * p.qscale;
         float alpha = 1.f;
         bool rescale = false;
         if (mx > m + 8.f) {
@@ -274,19 +325,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = kt > 0;
           m = mx;
         }
-        float rs = 0.f;
+        float rs8[8];
 #pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) {
+        for (int e = 0; e < 8; ++e) rs8[e] = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float p0 = ex2(fmaf(__uint_as_float(s[cc * 32 + 2 * e]), p.qscale, -m));
             const float p1 = ex2(fmaf(__uint_as_float(s[cc * 32 + 2 * e + 1]), p.qscale, -m));
-            rs += p0 + p1;
+            rs8[e & 7] += p0 + p1;
             pk[e] = pack_bf16x2(p0, p1);
           }
-          tmem_st16(tmem + lane_off + C::P_COL + sb * 64 + cc * 16, pk);
+          tmem_st16(tmem + lane_off + C::P_COL + sb * 64 + half * 32 + cc * 16, pk);
         }
+        const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         l = fmaf(l, alpha, rs);
         // tcgen05.ld / st are warp-collective: the whole warp rescales its O rows
         // when any of its rows raised the max (the others multiply by alpha = 1).
@@ -297,13 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < D / 64; ++c) {
             uint32_t o[32];
-            tmem_ld32(tmem + lane_off + C::O_COL + c * 32, o);
+            const uint32_t oc = tmem + lane_off + C::O_COL + half * (D / 2) + c * 32;
+            tmem_ld32(oc, o);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tmem + lane_off + C::O_COL + c * 32, o);
+            tmem_st32(oc, o);
           }
         }
         tmem_wait_st();
@@ -315,21 +370,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       // would return at once. o_last completes exactly once per item.
       if (!ok || !warp_wait(&bars->o_last, j & 1, p.err)) break;
       tc_fence_after();
-      uint32_t o[D];
+      uint32_t o[D / 2];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_off + C::O_COL + c * 32, o + c * 32);
+      for (int c = 0; c < D / 64; ++c)
+        tmem_ld32(tmem + lane_off + C::O_COL + half * (D / 2) + c * 32, o + c * 32);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars->o_free);  // O may be overwritten by the next item
+      // the row's sum is the sum of both halves
+      bars->xsum[half][r] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->ebar[quad]);
+      if (!warp_wait(&bars->ebar[quad], j & 1, p.err)) break;
+      l += bars->xsum[half ^ 1][r];
       if (qrow < p.T) {
         const float inv = 1.f / l;
-        float* orow = p.O + (static_cast<size_t>(row) * p.T + qrow) * D;
+        float* orow = p.O + (static_cast<size_t>(row) * p.T + qrow) * D + half * (D / 2);
 #pragma unroll
-        for (int e = 0; e < D; e += 4)
+        for (int e = 0; e < D / 2; e += 4)
           *reinterpret_cast<float4*>(orow + e) =
               make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
                           __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-        p.lse2[static_cast<size_t>(row) * p.Tp + qrow] = m + log2f(l);
+        if (half == 0) p.lse2[static_cast<size_t>(row) * p.Tp + qrow] = m + log2f(l);
       }
       g += nkt;
     }
@@ -349,20 +411,25 @@ struct ColCfg {
   static constexpr int TILE = BM * D * 2;
   static constexpr uint32_t TMEM_COLS = 256;   // two S^T buffers
   static constexpr size_t SMEM =
-      static_cast<size_t>(1 + QST) * TILE + QST * BM * sizeof(float) + 1024 + 1024;
+      static_cast<size_t>(1 + QST) * TILE + QST * BM * sizeof(float) + 1024 + 2048;
 };
 
 struct ColBars {
   uint64_t k_full, k_empty;
   uint64_t q_full[8], q_empty[8];
   uint64_t s_full[2], s_free[2];
+  uint64_t ebar[4];     // per lane quadrant, one phase per item: both halves' sums posted
+  float xsum[2][128];   // [half][key row]
   uint32_t tmem;
 };
+
+static_assert(sizeof(ColBars) <= 2048, "ColBars must fit the space reserved in ColCfg::SMEM");
 
 struct ColParams {
   const float* lse2;
   float* colsum;
   int rows, T, Tp, nqt, items;
+  int rb;  // rows per L2 block of the item order
   float qscale;
   int32_t* err;
 };
@@ -387,12 +454,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->k_empty, 1);
     for (int i = 0; i < C::QST; ++i) {
       mbar_init(&bars->q_full[i], 1);
-      mbar_init(&bars->q_empty[i], 1 + 4);  // MMA commit + one arrival per softmax warp
+      mbar_init(&bars->q_empty[i], 1 + 8);  // MMA commit + one arrival per softmax warp
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_free[i], 4);
+      mbar_init(&bars->s_free[i], 8);
     }
+    for (int i = 0; i < 4; ++i) mbar_init(&bars->ebar[i], 2);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -414,7 +482,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int j = 0;
       for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x, ++j) {
-        const int kt = it / p.rows, row = it % p.rows, nq = p.nqt - kt;
+        int row, kt;
+        item_coords(it, p.rows, p.nqt, p.rb, row, kt);
+        const int nq = p.nqt - kt;
         if (j > 0 && !mbar_wait(&bars->k_empty, (j - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&bars->k_full, C::TILE);
         load_tile<D>(sK, &tk, kt, row, &bars->k_full);
@@ -438,7 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int j = 0;
       for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x, ++j) {
-        const int nq = p.nqt - it / p.rows;
+        int row, kt;
+        item_coords(it, p.rows, p.nqt, p.rb, row, kt);
+        const int nq = p.nqt - kt;
         if (!mbar_wait(&bars->k_full, j & 1, p.err)) break;
         for (int i = 0; i < nq; ++i) {
           const uint32_t gq = g + i;
@@ -462,13 +534,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    const int quad = warp & 3;
+    // Two warps per TMEM lane quadrant, one per half of the 128 query columns;
+    // a thread sums its key's probabilities over its half, and the halves are
+    // added once per item.
+    const int sw = warp - 2;
+    const int quad = warp & 3, half = sw >> 2;
     const int r = quad * 32 + lane;  // key row within the tile
+    const int cb = half * 64;        // first query column of this half
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     uint32_t g = 0;
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x) {
-      const int kt = it / p.rows, row = it % p.rows, nq = p.nqt - kt;
+    int j = 0;
+    for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x, ++j) {
+      int row, kt;
+      item_coords(it, p.rows, p.nqt, p.rb, row, kt);
+      const int nq = p.nqt - kt;
       float acc = 0.f;
       for (int i = 0; i < nq; ++i) {
         const uint32_t gq = g + i;
@@ -478,9 +558,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        uint32_t s[BM];
-#pragma unroll
-        for (int c = 0; c < BM / 32; ++c) tmem_ld32(tmem + lane_off + sb * 128 + c * 32, s + c * 32);
+        uint32_t s[64];
+        tmem_ld32(tmem + lane_off + sb * 128 + cb, s);
+        tmem_ld32(tmem + lane_off + sb * 128 + cb + 32, s + 32);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -489,27 +569,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const float* L = sL + st * BM;
-        const int qvalid = min(BM, p.T - qt * BM);  // queries past the prompt end are padding
-        float a = 0.f;
-        if (i == 0 || qvalid < BM) {
-          const int c0 = i == 0 ? r : 0;  // diagonal tile: queries c >= r only
+        const float* L = sL + st * BM + cb;
+        const int qvalid = min(BM, p.T - qt * BM) - cb;  // queries past the prompt end are padding
+        // Eight independent sums; the LSE values come as float4 loads.
+        float a8[8];
 #pragma unroll
-          for (int c = 0; c < BM; ++c) {
-            const float e = ex2(fmaf(__uint_as_float(s[c]), p.qscale, -L[c]));
-            a += (c >= c0 && c < qvalid) ? e : 0.f;
+        for (int e = 0; e < 8; ++e) a8[e] = 0.f;
+        if (i == 0 || qvalid < 64) {
+          const int c0 = i == 0 ? r - cb : 0;  // diagonal tile: queries >= key r only
+#pragma unroll
+          for (int c4 = 0; c4 < 64; c4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(L + c4);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = c4 + e;
+              const float x = ex2(fmaf(__uint_as_float(s[c]), p.qscale, -lv[e]));
+              a8[c & 7] += (c >= c0 && c < qvalid) ? x : 0.f;
+            }
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < BM; ++c) a += ex2(fmaf(__uint_as_float(s[c]), p.qscale, -L[c]));
+          for (int c4 = 0; c4 < 64; c4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(L + c4);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = c4 + e;
+              a8[c & 7] += ex2(fmaf(__uint_as_float(s[c]), p.qscale, -lv[e]));
+            }
+          }
         }
-        acc += a;
+        acc += ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->q_empty[st]);
       }
       if (!ok) break;
+      // add the two halves
+      bars->xsum[half][r] = acc;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->ebar[quad]);
+      if (!warp_wait(&bars->ebar[quad], j & 1, p.err)) break;
       const int key = kt * BN + r;
-      if (key < p.T) p.colsum[static_cast<size_t>(row) * p.T + key] = acc;
+      if (half == 0 && key < p.T)
+        p.colsum[static_cast<size_t>(row) * p.T + key] = acc + bars->xsum[1][r];
       g += nq;
     }
   }
@@ -533,6 +636,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
   }
   return fn;
+}
+
+// Rows per block of the item order: `tensors` bf16 [T, D] operands re-read by
+// every item of a row (K and V for the forward pass, Q for the column sums)
+// should total about 24 MB per block, well inside the 129 MB L2.
+int rows_per_l2_block(int T, int D, int tensors) {
+  const double per_row = static_cast<double>(tensors) * T * D * 2;
+  const int rb = static_cast<int>(24.0e6 / per_row);
+  return rb < 1 ? 1 : rb;
 }
 
 // SM count of the current device (one persistent CTA per SM).
@@ -575,7 +687,8 @@ cudaError_t forward_t(const void* Q, const void* K, const void* V, int rows, int
     attr = true;
   }
   const int nqt = (T + BM - 1) / BM;
-  FwdParams p{O, lse2, rows, T, lse_stride(T), nqt, rows * nqt, kLog2e / sqrtf(float(D)), err};
+  FwdParams p{O, lse2, rows, T, lse_stride(T), nqt, rows * nqt, rows_per_l2_block(T, D, 2),
+              kLog2e / sqrtf(float(D)), err};
   const unsigned grid = static_cast<unsigned>(std::min(p.items, num_sms()));
   attn_fwd_kernel<D><<<grid, kThreads, FwdCfg<D>::SMEM, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
@@ -596,7 +709,8 @@ cudaError_t colsum_t(const void* Q, const void* K, const float* lse2, int rows, 
     attr = true;
   }
   const int nqt = (T + BM - 1) / BM;
-  ColParams p{lse2, colsum, rows, T, lse_stride(T), nqt, rows * nqt, kLog2e / sqrtf(float(D)), err};
+  ColParams p{lse2, colsum, rows, T, lse_stride(T), nqt, rows * nqt, rows_per_l2_block(T, D, 1),
+              kLog2e / sqrtf(float(D)), err};
   const unsigned grid = static_cast<unsigned>(std::min(p.items, num_sms()));
   attn_colsum_kernel<D><<<grid, kThreads, ColCfg<D>::SMEM, stream>>>(mq, mk, p);
   return cudaGetLastError();
