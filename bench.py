@@ -40,6 +40,7 @@ from workloads import (WORKLOADS, decode_bytes_per_row_step, head_direction,  # 
 METRIC = "H2O decode tokens/s/GPU at 20% KV budget; achieved HBM GB/s vs peak"
 UNIT = "tokens/s"
 PREFILL_LAUNCHES = 4  # forward, column sums, select, gather
+ORACLE_ROW_BLOCK = 1024  # query rows per block of the oracle's prefill
 
 
 # --------------------------------------------------------------------------- CPU oracle leg
@@ -52,9 +53,15 @@ def _oracle_rows_timed(job):
     w, rows_bits = job
     t0 = time.perf_counter()
     for q, k, v in rows_bits:
+        # row_block bounds the oracle's memory (a T x T block per call otherwise)
         oracle.run_row(bf16_bits_to_f64(q), bf16_bits_to_f64(k), bf16_bits_to_f64(v), w.prompt,
-                       w.steps, w.h, w.r, keep_sets=False)
+                       w.steps, w.h, w.r, row_block=ORACLE_ROW_BLOCK, keep_sets=False)
     return time.perf_counter() - t0
+
+
+def _oracle_row_flops(w):
+    """Rough fp64 work of one oracle row: causal prefill plus the decode steps."""
+    return 4 * w.head_dim * w.prompt * w.prompt + 4 * w.steps * w.k * w.head_dim
 
 
 def _sample_rows(w, n):
@@ -66,8 +73,10 @@ def _sample_rows(w, n):
 class OracleTimer:
     """Times the CPU oracle on sampled rows with one spawn process per core."""
 
-    def __init__(self, w, rows_per_core=2):
+    def __init__(self, w, rows_per_core=None):
         self.w = w
+        if rows_per_core is None:  # about 10-30 s of oracle work per run
+            rows_per_core = 2 if _oracle_row_flops(w) < 1e11 else 1
         self.cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
         self.pool = mp.get_context("spawn").Pool(self.cores)
         rows = _sample_rows(w, rows_per_core * self.cores)
@@ -79,14 +88,19 @@ class OracleTimer:
         t0 = time.perf_counter()
         self.pool.map(_oracle_rows_timed, self.jobs, chunksize=1)
         wall = time.perf_counter() - t0
-        tokens = len(self.rows) / self.w.heads * self.w.steps  # one token = all heads of a sequence
-        return tokens / wall, wall
+        return self.tokens() / wall, wall
+
+    def tokens(self):
+        """Decode tokens the sampled rows stand for: a token passes through every
+        head of every layer, so it is rows / (heads x layers) x steps."""
+        w = self.w
+        return len(self.rows) / (w.heads * w.layers) * w.steps
 
     def describe(self):
         w = self.w
         return (f"{len(self.rows)} of {w.batch * w.heads} (batch, head) rows of {w.name}, each a full "
                 f"prefill of {w.prompt} tokens plus {w.steps} decode steps; tokens counted as "
-                f"rows / heads x steps")
+                f"rows / (heads x layers) x steps")
 
     def close(self):
         self.pool.close()
@@ -206,7 +220,7 @@ def run_reference(args, w):
             walls.append(wall)
     finally:
         timer.close()
-    value = float(len(timer.rows) / w.heads * w.steps * args.steps / sum(walls))
+    value = float(timer.tokens() * args.steps / sum(walls))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(walls) / args.steps,
@@ -219,15 +233,62 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-def _config(w):
+MAX_DISTINCT_ROWS = 512    # distinct seeded rows per input layer; larger batches repeat them
+MAX_DISTINCT_LAYERS = 2    # distinct seeded input layers; deeper stacks cycle through them
+L2_FALLBACK_BYTES = 129 << 20
+MAX_CYCLED_LAYERS = 64     # tiny caches stay latency-bound; they are not cycled
+
+
+def _layer_cache_bytes(w):
+    """Device bytes of one layer's cache: K, V (bf16), score (fp32), position (int32)."""
+    return w.rows_per_layer * w.k * (4 * w.head_dim + 8)
+
+
+def _default_steps(w):
+    """Timed steps so that the timed region stays within about 20 s (3 .. 200)."""
+    est = (w.layers * w.steps * decode_bytes_per_row_step(w.k, w.head_dim) * w.rows_per_layer / 4e12
+           + w.layers * prefill_flops_per_row(w.prompt, w.head_dim) * w.rows_per_layer / 3e14)
+    return int(max(3, min(200, 20.0 / max(est, 1e-9))))
+
+
+def _data_desc(w):
+    rows, layers = w.rows_per_layer, w.layers
+    s = "synthetic: seeded N(0,1) q/k/v plus a power-law shared key direction per head; no weights"
+    if rows > MAX_DISTINCT_ROWS:
+        s += f"; {MAX_DISTINCT_ROWS} distinct seeded rows per layer, repeated over the {rows} rows"
+    if layers > MAX_DISTINCT_LAYERS:
+        s += (f"; {MAX_DISTINCT_LAYERS} distinct seeded input layers cycled over the {layers} "
+              "layers (each layer keeps its own cache)")
+    return s
+
+
+def _config(w, l2_bytes=L2_FALLBACK_BYTES):
+    cache = _layer_cache_bytes(w) * w.layers
+    l2 = ("inputs larger than L2 (prompt Q/K/V read every step); "
+          + ("the decode caches of all layers exceed L2" if cache > l2_bytes else
+             "the decode cache fits in L2 and stays resident across the decode steps of a step "
+             "(roofline.achieved_l2_cycled gives the L2-cold figure)"))
     return {"workload": w.name, "layers": w.layers, "batch": w.batch, "heads": w.heads,
             "head_dim": w.head_dim, "prompt": w.prompt, "decode_steps": w.steps, "h": w.h, "r": w.r,
             "zipf_alpha": w.alpha,
-            "step": f"prefill of {w.prompt} tokens + {w.steps} decode steps (CUDA graph)",
+            "step": (f"prefill of {w.prompt} tokens for each of {w.layers} layer(s), then "
+                     f"{w.steps} decode steps through every layer (one CUDA graph)"),
             "tokens_per_step": w.batch * w.steps,
-            "l2": "inputs larger than L2 (prompt Q/K/V read every step); the decode cache stays "
-                  "L2-resident across the decode steps of a step",
-            "parallelism": "one replica per GPU (independent batches)"}
+            "l2": l2, "parallelism": "one replica per GPU (independent batches)"}
+
+
+def _gen_layer(w, seed_layer):
+    """bf16 bits [3, B, H, N, d] of one input layer (rows beyond MAX_DISTINCT_ROWS repeat)."""
+    B, H, N, d = w.batch, w.heads, w.tokens, w.head_dim
+    bits = np.empty((3, B * H, N, d), dtype=np.uint16)
+    dirs = [head_direction(w, seed_layer, j) for j in range(H)]
+    nd = min(B * H, MAX_DISTINCT_ROWS)
+    for i in range(nd):
+        b, j = divmod(i, H)
+        bits[:, i] = np.stack(row_tokens(w, seed_layer, b, j, dirs[j]))
+    for i in range(nd, B * H):
+        bits[:, i] = bits[:, i % nd]
+    return bits.reshape(3, B, H, N, d)
 
 
 # --------------------------------------------------------------------------- our arm
@@ -235,9 +296,7 @@ def run_ours(args, w):
     import torch
 
     ws, rank, local = _dist_env()
-    timer = OracleTimer(w) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
-    if ws > 1 and rank == 0 and not args.no_cpu_baseline:
-        timer = OracleTimer(w)
+    timer = OracleTimer(w) if (rank == 0 and not args.no_cpu_baseline) else None
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pg = None
@@ -250,46 +309,58 @@ def run_ours(args, w):
     build()
     import h2o_heavy_hitter_gb300 as h2o
 
-    B, H, d, T, S = w.batch, w.heads, w.head_dim, w.prompt, w.steps
-    N = w.tokens
-    # Inputs: each rank draws its own layer seed (independent batches).
+    B, H, d, T, S, L = w.batch, w.heads, w.head_dim, w.prompt, w.steps, w.layers
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)
+                   or L2_FALLBACK_BYTES)
+    # Inputs: each rank draws its own seeds (independent batches).
     t0 = time.perf_counter()
-    bits = np.empty((3, B, H, N, d), dtype=np.uint16)
-    seed_layer = rank_layer_seed(rank)
-    dirs = [head_direction(w, seed_layer, j) for j in range(H)]
-    for b in range(B):
-        for j in range(H):
-            q, k, v = row_tokens(w, seed_layer, b, j, dirs[j])
-            bits[0, b, j], bits[1, b, j], bits[2, b, j] = q, k, v
-    gen_s = time.perf_counter() - t0
+    nl = min(L, MAX_DISTINCT_LAYERS)
 
     def host(x):
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
 
-    hp = [host(bits[i][:, :, :T]).pin_memory() for i in range(3)]  # prompt [B,H,T,d]
-    hs = [host(bits[i][:, :, T:].transpose(2, 0, 1, 3)).pin_memory() for i in range(3)]  # [S,B,H,d]
-    dp = [x.to(dev) for x in hp]
-    ds = [x.to(dev) for x in hs]
+    hp, hs = [], []  # per input layer: prompt [B,H,T,d] x3, decode inputs [S,B,H,d] x3 (pinned)
+    for li in range(nl):
+        bits = _gen_layer(w, rank_layer_seed(rank) * MAX_DISTINCT_LAYERS + li)
+        hp.append([host(bits[i][:, :, :T]).pin_memory() for i in range(3)])
+        hs.append([host(bits[i][:, :, T:].transpose(2, 0, 1, 3)).pin_memory() for i in range(3)])
+        del bits
+    gen_s = time.perf_counter() - t0
+    dp = [[x.to(dev) for x in lay] for lay in hp]
+    ds = [[x.to(dev) for x in lay] for lay in hs]
+    # One output buffer per phase, written by every layer in turn (a following
+    # model layer would consume it); the last layer's values are the step's result.
     pre_out = torch.empty((B, H, T, d), dtype=torch.float32, device=dev)
     dec_out = torch.empty((S, B, H, d), dtype=torch.float32, device=dev)
     h_pre_out = torch.empty(pre_out.shape, dtype=torch.float32).pin_memory()
     h_dec_out = torch.empty(dec_out.shape, dtype=torch.float32).pin_memory()
 
-    ctx = h2o.h2o_create(1, B, H, d, w.h, w.r)
+    ctx = h2o.h2o_create(L, B, H, d, w.h, w.r)
     stream = torch.cuda.Stream(device=dev)
+
+    def prefill_all(c, layers):
+        for layer in range(layers):
+            h2o.h2o_prefill(c, layer, *dp[layer % nl], out=pre_out)
+
+    def capture(c, layers, steps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for s in range(steps):
+                for layer in range(layers):
+                    x = ds[layer % nl]
+                    h2o.h2o_decode_step(c, layer, x[0][s], x[1][s], x[2][s], dec_out[s])
+        return g
+
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        h2o.h2o_prefill(ctx, 0, *dp, out=pre_out)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for s in range(S):
-                h2o.h2o_decode_step(ctx, 0, ds[0][s], ds[1][s], ds[2][s], dec_out[s])
+        prefill_all(ctx, L)
+        graph = capture(ctx, L, S)
     torch.cuda.synchronize()
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        h2o.h2o_prefill(ctx, 0, *dp, out=pre_out)
+        prefill_all(ctx, L)
         if ev is not None:
             ev[1].record(stream)
         graph.replay()
@@ -326,14 +397,13 @@ def run_ours(args, w):
     decode_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
 
     # ---- end-to-end through the public API with host buffers
-    h2d = sum(x.numel() * 2 for x in hp + hs)
+    h2d = sum(x.numel() * 2 for lay in hp + hs for x in lay)
     d2h = (pre_out.numel() + dec_out.numel()) * 4
 
     def e2e_step():
-        for dst, src in zip(dp, hp):
-            dst.copy_(src, non_blocking=True)
-        for dst, src in zip(ds, hs):
-            dst.copy_(src, non_blocking=True)
+        for dl, hl in zip(dp + ds, hp + hs):
+            for dst, src in zip(dl, hl):
+                dst.copy_(src, non_blocking=True)
         step()
         h_pre_out.copy_(pre_out, non_blocking=True)
         h_dec_out.copy_(dec_out, non_blocking=True)
@@ -351,29 +421,54 @@ def run_ours(args, w):
         e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), pg, dev)
+    del graph
 
-    # ---- decode launches with L2 flushed before each (HBM-cold reference point).
-    # The flush writes a buffer twice the size of L2 and then reads it back, so
-    # L2 holds clean lines: the timed kernel pays no write-back of dirty data.
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    ctx_l2 = h2o.h2o_create(1, B, H, d, w.h, w.r)
-    with torch.cuda.stream(stream):
-        h2o.h2o_prefill(ctx_l2, 0, *dp, out=pre_out)
+    # ---- decode with the caches cycled through L2: when one layer's caches fit
+    # in L2, a graph of decode steps over enough copies of the layer (more than
+    # twice the L2 size in all) makes every launch read its cache from HBM, as
+    # the layers of a deep model would, with launches still back to back.
+    cycled_ms, n_cycle = None, 0
+    need = -(-2 * l2_bytes // _layer_cache_bytes(w))
+    if _layer_cache_bytes(w) * L <= l2_bytes and need <= MAX_CYCLED_LAYERS:
+        n_cycle = max(2, need)
+        ctx_c = h2o.h2o_create(n_cycle, B, H, d, w.h, w.r)
+        sc = min(S, 32)
+        with torch.cuda.stream(stream):
+            prefill_all(ctx_c, n_cycle)
+            g_c = capture(ctx_c, n_cycle, sc)
+            prefill_all(ctx_c, n_cycle)
+            g_c.replay()  # warm-up replay
+            prefill_all(ctx_c, n_cycle)
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            g_c.replay()
+            c1.record(stream)
+        torch.cuda.synchronize()
+        cycled_ms = c0.elapsed_time(c1) / (sc * n_cycle)
+        del g_c
+        h2o.h2o_sync_check(ctx_c)
+        ctx_c.close()
+
+    # ---- single decode launches with L2 flushed before each (HBM-cold and
+    # launch-isolated: the pessimistic reference point). The flush writes a
+    # buffer twice the size of L2 and reads it back, so L2 holds clean lines.
+    flush = torch.empty(max(256 << 20, 2 * l2_bytes), dtype=torch.uint8, device=dev)
     cold = []
     n_cold = min(S, 64)
     with torch.cuda.stream(stream):
+        prefill_all(ctx, L)
         for s in range(n_cold):
             flush.fill_(s & 0xff)
             flush.sum(dtype=torch.int64)
             a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            h2o.h2o_decode_step(ctx_l2, 0, ds[0][s], ds[1][s], ds[2][s], dec_out[s])
+            x = ds[0]
+            h2o.h2o_decode_step(ctx, 0, x[0][s], x[1][s], x[2][s], dec_out[s])
             b_.record(stream)
             cold.append((a, b_))
     torch.cuda.synchronize()
     cold_ms = float(np.mean([a.elapsed_time(b_) for a, b_ in cold[1:]]))
-    h2o.h2o_sync_check(ctx_l2)
-    ctx_l2.close()
+    del flush
     h2o.h2o_sync_check(ctx)
     ctx.close()
 
@@ -385,37 +480,41 @@ def run_ours(args, w):
     peaks, peak_kind = _peaks()
     rows = B * H
     bytes_per_launch = decode_bytes_per_row_step(w.k, d) * rows
-    dec_launch_ms = decode_ms / S  # graph replay: launch gaps included
+    dec_launch_ms = decode_ms / (S * L)  # graph replay: launch gaps included
     achieved = bytes_per_launch / (dec_launch_ms * 1e-3) / 1e9
     achieved_cold = bytes_per_launch / (cold_ms * 1e-3) / 1e9
     hbm = float(peaks["hbm_gbs"])
-    pflops = prefill_flops_per_row(T, d) * rows
+    pflops = prefill_flops_per_row(T, d) * rows * L
     pre_tflops = pflops / (prefill_ms * 1e-3) / 1e12
     tokens = B * S * args.steps * ws
     value = tokens / (elapsed_ms * 1e-3)
+    roof = {"kernel": "h2o decode_kernel", "bound": "hbm", "achieved": achieved,
+            "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": _profiled_traffic("decode.cu", w.name),
+            "bytes_per_launch": bytes_per_launch,
+            "launch_ms": dec_launch_ms,
+            "peak_source": f"{peak_kind} hbm_gbs"}
+    if cycled_ms is not None:
+        a_c = bytes_per_launch / (cycled_ms * 1e-3) / 1e9
+        roof.update({"achieved_l2_cycled": a_c, "frac_l2_cycled": a_c / hbm,
+                     "launch_ms_l2_cycled": cycled_ms, "l2_cycled_layers": n_cycle})
+    roof.update({"achieved_l2_flushed": achieved_cold, "frac_l2_flushed": achieved_cold / hbm,
+                 "launch_ms_l2_flushed": cold_ms})
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic: seeded N(0,1) q/k/v plus a power-law shared key direction per head; no weights",
-        "config": _config(w),
-        "roofline": {"kernel": "h2o decode_kernel", "bound": "hbm", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": _profiled_traffic("decode.cu", w.name),
-                     "bytes_per_launch": bytes_per_launch,
-                     "launch_ms": dec_launch_ms,
-                     "peak_source": f"{peak_kind} hbm_gbs",
-                     "achieved_l2_flushed": achieved_cold, "frac_l2_flushed": achieved_cold / hbm,
-                     "launch_ms_l2_flushed": cold_ms},
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": _data_desc(w),
+        "config": _config(w, l2_bytes),
+        "roofline": roof,
         "phases": {"prefill_ms": prefill_ms, "decode_ms": decode_ms,
-                   "prefill_tokens_per_s": B * T / (prefill_ms * 1e-3),
+                   "prefill_tokens_per_s": B * T * L / (prefill_ms * 1e-3),
                    "prefill_tflops": pre_tflops,
                    "prefill_frac_bf16": pre_tflops / float(peaks["bf16_tflops"]),
                    "decode_only_tokens_per_s": B * S / (decode_ms * 1e-3),
                    "input_generation_s": gen_s},
         "e2e": {"value": B * S * e2e_steps * ws / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": (PREFILL_LAUNCHES + S) * args.steps,
+        "gpu_launches": (PREFILL_LAUNCHES + S) * L * args.steps,
         "clocks": clk,
     }
     if timer is not None:
@@ -431,7 +530,8 @@ def run_ours(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 200, fewer for heavy workloads)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="opt-6.7b-layer", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -440,6 +540,8 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     w = WORKLOADS[args.workload]
+    if args.steps is None:
+        args.steps = _default_steps(w)
     if args.impl == "reference":
         run_reference(args, w)
     else:
