@@ -6,23 +6,27 @@
 // Two passes over the causal (query, key) tile pairs, 128 x 128 tiles:
 //   forward: one item per (row, query tile). S = Q K^T in TMEM (tcgen05.mma, bf16
 //            operands staged by TMA with 128-byte swizzle), online softmax in
-//            registers (one thread per query row, base-2 logits), P written
-//            back to TMEM as bf16 (its own double buffer, never aliased with
-//            S) and O += P V issued with P as the TMEM operand. The running
+//            registers (one thread per query row and half of the keys,
+//            base-2 logits), P written back as bf16 over the S columns it came
+//            from, and O += P V issued with P as the TMEM operand. The running
 //            max is only raised when it grows by more than 2^8, so O is rarely
-//            rescaled. Writes O (fp32) and the base-2 log-sum-exp of every
-//            query row.
+//            rescaled. O is double-buffered in TMEM by item, so dedicated
+//            epilogue warps normalise and store item j (TMA stores through a
+//            small staging tile) while item j + 1 runs. Writes O (fp32) and
+//            the base-2 log-sum-exp of every query row.
 //   colsum:  one item per (row, key tile). S^T = K Q^T in TMEM (one thread per
-//            key row), P = 2^(s - lse2) with the finished row statistics, and
-//            each thread sums its key's probabilities over all later queries.
+//            key row) with the key tile held in TMEM as the A operand, so each
+//            MMA reads only the query tile from shared memory; P = 2^(s - lse2)
+//            with the finished row statistics, and each thread sums its key's
+//            probabilities over all later queries.
 // The column sums need every row's final normaliser, so the second pass
 // recomputes QK^T (1.5x the algorithmic flops) rather than storing T^2 values.
 //
 // Both kernels are persistent (one CTA per SM walking a longest-first item
-// list). Warp roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM
-// and issues the MMAs, warps 2-5 (one per TMEM lane quadrant) do the softmax.
-// Every mbarrier wait is bounded; a wait that gives up sets the device error
-// word and the CTA unwinds, always freeing its Tensor Memory.
+// list) and warp-specialised: TMA producer warps, one MMA warp that owns the
+// TMEM, softmax warps (two per TMEM lane quadrant) and, in the forward pass,
+// epilogue warps. Every mbarrier wait is bounded; a wait that gives up sets
+// the device error word and the CTA unwinds, always freeing its Tensor Memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -39,20 +43,58 @@ namespace {
 
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per tile
-constexpr int kThreads = 320;        // 10 warps: TMA, MMA, 8 softmax
-constexpr int kSoftmaxThreads = 256;
 constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16
+
+// ---- bulk async stores (TMA engine, shared -> global) ---------------------------
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0,
+                                             int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The shared-memory source of every committed store has been read.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Every committed store has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy reads.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ forward
+// Warp roles of the forward kernel (15 warps).
+constexpr int kWarpQK = 0;        // TMA loads of Q and K
+constexpr int kWarpMMA = 1;       // owns TMEM, issues every tcgen05.mma
+constexpr int kWarpSoftmax0 = 2;  // warps 2..9: softmax, two per TMEM lane quadrant
+constexpr int kWarpEpi0 = 10;     // warps 10..13: epilogue, one per lane quadrant
+constexpr int kWarpV = 14;        // TMA loads of V
+constexpr int kFwdThreads = 15 * 32;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kEpiWarps = 4;
 
 template <int D>
 struct FwdCfg {
   static constexpr int KST = D == 128 ? 3 : 4;  // K tiles in flight
   static constexpr int VST = D == 128 ? 2 : 3;  // V tiles in flight
   static constexpr int TILE = BM * D * 2;
-  static constexpr uint32_t S_COL = 0;    // two S buffers: columns [0, 128) and [128, 256)
-  static constexpr uint32_t O_COL = 256;  // O: columns [256, 256 + D)
-  static constexpr uint32_t P_COL = 384;  // two bf16 P buffers: columns [384, 448) and [448, 512)
+  // TMEM: S buffers b = 0, 1 at columns [128 b, 128 b + 128); the bf16 P of a
+  // tile overwrites its own S buffer (keys [64 h, 64 h + 64) at columns
+  // 64 h + [0, 32)); O buffers by item parity at 256 + 128 b.
+  static constexpr uint32_t S_COL = 0;
+  static constexpr uint32_t O_COL = 256;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr size_t SMEM = static_cast<size_t>(1 + KST + VST) * TILE + 1024 + 4096;
+  static constexpr int STAGE_BYTES = 32 * 32 * 4;  // epilogue staging per warp: 32 rows x 32 fp32
+  static constexpr size_t TILES = static_cast<size_t>(1 + KST + VST) * TILE;
+  static constexpr size_t SMEM = TILES + kEpiWarps * STAGE_BYTES + 1024 + 6144;
 };
 
 struct FwdBars {
@@ -60,20 +102,20 @@ struct FwdBars {
   uint64_t k_full[4], k_empty[4];
   uint64_t v_full[4], v_empty[4];
   uint64_t s_full[2], p_ready[2];
-  uint64_t o_done;  // one phase per PV (waited only by the rare O rescale)
-  uint64_t o_last;  // one phase per item: its last PV has completed
-  uint64_t o_free;  // one phase per item: the epilogue has read O out of TMEM
-  uint64_t xbar[4];  // per lane quadrant, one phase per tile: both halves' maxima posted
-  uint64_t ebar[4];  // per lane quadrant, one phase per item: both halves' sums posted
+  uint64_t o_done;      // one phase per PV (waited only by the rare O rescale)
+  uint64_t o_last[2];   // per O buffer, one phase per item: the item's last PV completed
+  uint64_t o_free[2];   // per O buffer, one phase per item: the epilogue read O out of TMEM
+  uint64_t l_ready[2];  // per O buffer, one phase per item: row sums and maxima posted
+  uint64_t xbar[4];     // per lane quadrant, one phase per tile: both halves' maxima posted
   float xmax[2][2][128];  // [tile parity][half][row]
-  float xsum[2][128];     // [half][row]
+  float lsum[2][2][128];  // [O buffer][half][row]: the half's row sum
+  float lmax[2][128];     // [O buffer][row]: the row's final running max (base-2 units)
   uint32_t tmem;
 };
 
-static_assert(sizeof(FwdBars) <= 4096, "FwdBars must fit the space reserved in FwdCfg::SMEM");
+static_assert(sizeof(FwdBars) <= 6144, "FwdBars must fit the space reserved in FwdCfg::SMEM");
 
 struct FwdParams {
-  float* O;
   float* lse2;
   int rows, T, Tp, nqt, items;
   int rb;  // rows per L2 block of the item order
@@ -93,9 +135,9 @@ __device__ __forceinline__ void load_tile(void* dst, const CUtensorMap* map, int
     tma_load_3d(static_cast<uint8_t*>(dst) + b * kBoxBytes, map, b * 64, tile * 128, row, bar);
 }
 
-// Wait used by the softmax warps: the result is made warp-uniform, so a wait
-// that gives up in one lane never leaves the warp to run a warp-collective
-// tcgen05.ld / st divergently.
+// Wait used by warps that go on to run warp-collective tcgen05.ld / st: the
+// result is made warp-uniform, so a wait that gives up in one lane never
+// leaves the warp to run them divergently.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
 }
@@ -125,18 +167,21 @@ __device__ __forceinline__ uint64_t desc_kmajor(const uint8_t* tile, int kk) {
 // Persistent: CTA b takes work items b, b + grid, ... of a list ordered by
 // decreasing work (query tile nqt-1 of every row first). Barrier phases run on
 // per-CTA counters that every role advances identically: g = K/V tiles so far,
-// j = items so far.
+// j = items so far. Item j accumulates into O buffer j & 1, so the epilogue
+// warps read item j out of TMEM while item j + 1 already runs.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                    const FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sQ = smem;
   uint8_t* sK = smem + C::TILE;
   uint8_t* sV = smem + (1 + C::KST) * C::TILE;
-  FwdBars* bars = reinterpret_cast<FwdBars*>(smem + (1 + C::KST + C::VST) * C::TILE);
+  uint8_t* sStage = smem + C::TILES;
+  FwdBars* bars = reinterpret_cast<FwdBars*>(sStage + kEpiWarps * C::STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -153,32 +198,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_ready[i], kSoftmaxThreads);
+      mbar_init(&bars->o_last[i], 1);
+      mbar_init(&bars->o_free[i], kEpiWarps);
+      mbar_init(&bars->l_ready[i], kSoftmaxThreads / 32);
     }
     mbar_init(&bars->o_done, 1);
-    mbar_init(&bars->o_last, 1);
-    mbar_init(&bars->o_free, kSoftmaxThreads);
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&bars->xbar[i], 2);
-      mbar_init(&bars->ebar[i], 2);
-    }
+    for (int i = 0; i < 4; ++i) mbar_init(&bars->xbar[i], 2);
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (warp == kWarpMMA) {
     tmem_alloc(&bars->tmem, C::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == kWarpQK && lane == 0) {
     tma_prefetch_map(&tq);
     tma_prefetch_map(&tk);
-    tma_prefetch_map(&tv);
+    tma_prefetch_map(&to);
   }
+  if (warp == kWarpV && lane == 0) tma_prefetch_map(&tv);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
+  if (warp == kWarpQK) {
+    // ---------------------------------------------------------------- TMA: Q and K
     if (lane == 0) {
       uint32_t g = 0;
       bool ok = true;
@@ -191,13 +235,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&bars->q_full, C::TILE);
         load_tile<D>(sQ, &tq, qt, row, &bars->q_full);
         for (int kt = 0; kt <= qt; ++kt, ++g) {
-          const int ks = g % C::KST, vs = g % C::VST;
+          const int ks = g % C::KST;
           if (g >= C::KST && !mbar_wait(&bars->k_empty[ks], ((g / C::KST) - 1) & 1, p.err)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&bars->k_full[ks], C::TILE);
           load_tile<D>(sK + ks * C::TILE, &tk, kt, row, &bars->k_full[ks]);
+        }
+      }
+    }
+  } else if (warp == kWarpV) {
+    // ---------------------------------------------------------------- TMA: V
+    // Its own warp, so K tiles are never held back by a wait for a V stage.
+    if (lane == 0) {
+      uint32_t g = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x) {
+        int row, rank;
+        item_coords(it, p.rows, p.nqt, p.rb, row, rank);
+        const int qt = p.nqt - 1 - rank;
+        for (int kt = 0; kt <= qt; ++kt, ++g) {
+          const int vs = g % C::VST;
           if (g >= C::VST && !mbar_wait(&bars->v_empty[vs], ((g / C::VST) - 1) & 1, p.err)) {
             ok = false;
             break;
@@ -207,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpMMA) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, 0, 0);
@@ -219,9 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         int row, rank;
         item_coords(it, p.rows, p.nqt, p.rb, row, rank);
         const int nkt = p.nqt - rank;
+        const int ob = j & 1;
         if (!mbar_wait(&bars->q_full, j & 1, p.err)) break;
         for (int kt = 0; kt <= nkt; ++kt) {
           if (kt < nkt) {
+            // S(gk) overwrites S/P(gk - 2), whose PV was issued before it:
+            // the MMAs of this thread run in issue order.
             const uint32_t gk = g + kt;
             const int ks = gk % C::KST, sb = gk & 1;
             if (!mbar_wait(&bars->k_full[ks], (gk / C::KST) & 1, p.err)) {
@@ -243,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int pb = gp & 1, vs = gp % C::VST;
             if (!mbar_wait(&bars->p_ready[pb], (gp >> 1) & 1, p.err) ||
                 !mbar_wait(&bars->v_full[vs], (gp / C::VST) & 1, p.err) ||
-                (kt == 1 && j > 0 && !mbar_wait(&bars->o_free, (j - 1) & 1, p.err))) {
+                (kt == 1 && j >= 2 && !mbar_wait(&bars->o_free[ob], ((j >> 1) - 1) & 1, p.err))) {
               ok = false;
               break;
             }
@@ -254,24 +316,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               // B = V tile, MN-major: 16 keys = two 8-row swizzle atoms (2048 B);
               // the two 64-column halves of d sit one TMA box (16 KB) apart.
               const uint64_t bdesc = smem_desc(v_tile + kk * 2048, kBoxBytes, 1024);
-              umma_ts(tmem + C::O_COL, tmem + C::P_COL + pb * 64 + kk * 8, bdesc, idesc_pv,
+              const uint32_t a_tmem = tmem + C::S_COL + pb * 128 + (kk >> 2) * 64 + (kk & 3) * 8;
+              umma_ts(tmem + C::O_COL + ob * 128, a_tmem, bdesc, idesc_pv,
                       (kt > 1 || kk > 0) ? 1u : 0u);
             }
             umma_commit(&bars->v_empty[vs]);
             umma_commit(&bars->o_done);
-            if (kt == nkt) umma_commit(&bars->o_last);
+            if (kt == nkt) umma_commit(&bars->o_last[ob]);
           }
         }
         g += nkt;
       }
     }
-  } else {
+  } else if (warp < kWarpEpi0) {
     // ---------------------------------------------------------------- softmax
     // Two warps per TMEM lane quadrant, one per half of the 128 S columns; a
     // thread owns one query row's half. The halves share the row's running max
-    // (tile maxima exchanged through shared memory every tile) and add their
-    // row sums at the end of the item.
-    const int sw = warp - 2;
+    // (tile maxima exchanged through shared memory every tile); at the end of
+    // an item each posts its row sum for the epilogue warps.
+    const int sw = warp - kWarpSoftmax0;
     const int quad = warp & 3, half = sw >> 2;
     const int r = quad * 32 + lane;
     const int cb = half * 64;  // first S column of this half
@@ -283,19 +346,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       int row, rank;
       item_coords(it, p.rows, p.nqt, p.rb, row, rank);
       const int qt = p.nqt - 1 - rank;
-      const int nkt = qt + 1, qrow = qt * BM + r;
+      const int nkt = qt + 1;
+      const int ob = j & 1;
       float m = -INFINITY, l = 0.f;
       for (int kt = 0; kt < nkt; ++kt) {
         const uint32_t gs = g + kt;
         const int sb = gs & 1;
+        const uint32_t s_tm = tmem + lane_off + C::S_COL + sb * 128;
         if (!warp_wait(&bars->s_full[sb], (gs >> 1) & 1, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
         uint32_t s[64];
-        tmem_ld32(tmem + lane_off + C::S_COL + sb * 128 + cb, s);
-        tmem_ld32(tmem + lane_off + C::S_COL + sb * 128 + cb + 32, s + 32);
+        tmem_ld32(s_tm + cb, s);
+        tmem_ld32(s_tm + cb + 32, s + 32);
         tmem_wait_ld();
         if (kt == qt) {  // diagonal tile: key c is visible to query r iff c <= r
 #pragma unroll
@@ -338,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             rs8[e & 7] += p0 + p1;
             pk[e] = pack_bf16x2(p0, p1);
           }
-          tmem_st16(tmem + lane_off + C::P_COL + sb * 64 + half * 32 + cc * 16, pk);
+          // P overwrites the S columns this warp has already read
+          tmem_st16(s_tm + half * 64 + cc * 16, pk);
         }
         const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         l = fmaf(l, alpha, rs);
@@ -353,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < D / 64; ++c) {
             uint32_t o[32];
-            const uint32_t oc = tmem + lane_off + C::O_COL + half * (D / 2) + c * 32;
+            const uint32_t oc = tmem + lane_off + C::O_COL + ob * 128 + half * (D / 2) + c * 32;
             tmem_ld32(oc, o);
             tmem_wait_ld();
 #pragma unroll
@@ -365,65 +431,106 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&bars->p_ready[sb]);
       }
-      // o_done cannot be used here: when the softmax of the last tile ends, the
-      // PV of the tile before may still run, and a parity wait two phases back
-      // would return at once. o_last completes exactly once per item.
-      if (!ok || !warp_wait(&bars->o_last, j & 1, p.err)) break;
-      tc_fence_after();
-      uint32_t o[D / 2];
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tmem_ld32(tmem + lane_off + C::O_COL + half * (D / 2) + c * 32, o + c * 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars->o_free);  // O may be overwritten by the next item
-      // the row's sum is the sum of both halves
-      bars->xsum[half][r] = l;
+      if (!ok) break;
+      // Hand the row statistics to the epilogue. The slots of this O buffer
+      // were last read by the epilogue of item j - 2.
+      if (j >= 2 && !warp_wait(&bars->o_free[ob], ((j >> 1) - 1) & 1, p.err)) break;
+      bars->lsum[ob][half][r] = l;
+      if (half == 0) bars->lmax[ob][r] = m;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->ebar[quad]);
-      if (!warp_wait(&bars->ebar[quad], j & 1, p.err)) break;
-      l += bars->xsum[half ^ 1][r];
-      if (qrow < p.T) {
-        const float inv = 1.f / l;
-        float* orow = p.O + (static_cast<size_t>(row) * p.T + qrow) * D + half * (D / 2);
-#pragma unroll
-        for (int e = 0; e < D / 2; e += 4)
-          *reinterpret_cast<float4*>(orow + e) =
-              make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
-                          __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-        if (half == 0) p.lse2[static_cast<size_t>(row) * p.Tp + qrow] = m + log2f(l);
-      }
+      if (lane == 0) mbar_arrive(&bars->l_ready[ob]);
       g += nkt;
     }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    // One warp per lane quadrant: reads the item's O rows out of TMEM in
+    // 32-column chunks, normalises them and writes them with TMA stores
+    // through a 4 KB staging tile (128-byte swizzle: chunk q of row i at
+    // ((q ^ (i & 7)) * 16), which keeps the shared-memory writes conflict free).
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    uint8_t* stg = sStage + (warp - kWarpEpi0) * C::STAGE_BYTES;
+    int j = 0;
+    for (int it = blockIdx.x; it < p.items; it += gridDim.x, ++j) {
+      int row, rank;
+      item_coords(it, p.rows, p.nqt, p.rb, row, rank);
+      const int qt = p.nqt - 1 - rank;
+      const int ob = j & 1;
+      const int qrow = qt * BM + r;
+      const int tok0 = qt * BM + quad * 32;  // first token of this warp's rows
+      if (!warp_wait(&bars->o_last[ob], (j >> 1) & 1, p.err) ||
+          !warp_wait(&bars->l_ready[ob], (j >> 1) & 1, p.err))
+        break;
+      tc_fence_after();
+      const float lrow = bars->lsum[ob][0][r] + bars->lsum[ob][1][r];
+      const float inv = 1.f / lrow;
+      if (qrow < p.T) p.lse2[static_cast<size_t>(row) * p.Tp + qrow] = bars->lmax[ob][r] + log2f(lrow);
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + C::O_COL + ob * 128 + c * 32, o);
+        tmem_wait_ld();
+        if (c == D / 32 - 1) {  // O buffer fully read: the item after next may use it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->o_free[ob]);
+        }
+        if (lane == 0) bulk_wait_read_all();  // the previous store has read the staging tile
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(stg + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+              make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
+                          __uint_as_float(o[4 * q + 2]) * inv, __uint_as_float(o[4 * q + 3]) * inv);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && tok0 < p.T) {  // rows past the prompt end are clipped by the map
+          tma_store_3d(&to, stg, c * 32, tok0, row);
+          bulk_commit();
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kWarpMMA) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
 // ------------------------------------------------------------------ column sums
+constexpr int kColThreads = 320;  // warps: 0 TMA, 1 MMA, 2-9 softmax (two per lane quadrant)
+
 template <int D>
 struct ColCfg {
-  static constexpr int QST = D == 128 ? 4 : 6;  // query tiles in flight
+  static constexpr int KST = 2;                 // key tiles staged in shared memory
+  static constexpr int QST = D == 128 ? 4 : 8;  // query tiles in flight
+  static constexpr int LST = 8;                 // LSE slices in flight
   static constexpr int TILE = BM * D * 2;
-  static constexpr uint32_t TMEM_COLS = 256;   // two S^T buffers
+  // TMEM: S^T buffers at columns [0, 128) and [128, 256); the key tile as the
+  // MMA's A operand (bf16 pairs, one key per lane) in two buffers of D/2
+  // columns from column 256, by item parity.
+  static constexpr uint32_t KA_COL = 256;
+  static constexpr uint32_t TMEM_COLS = 512;
   static constexpr size_t SMEM =
-      static_cast<size_t>(1 + QST) * TILE + QST * BM * sizeof(float) + 1024 + 2048;
+      static_cast<size_t>(KST + QST) * TILE + LST * BM * sizeof(float) + 1024 + 4096;
 };
 
 struct ColBars {
-  uint64_t k_full, k_empty;
+  uint64_t k_full[2], k_empty[2];  // key tile staged in shared memory / copied out of it
+  uint64_t ka_full[2];             // key tile written into TMEM (A operand), by item parity
   uint64_t q_full[8], q_empty[8];
+  uint64_t l_full[8], l_empty[8];
   uint64_t s_full[2], s_free[2];
   uint64_t ebar[4];     // per lane quadrant, one phase per item: both halves' sums posted
-  float xsum[2][128];   // [half][key row]
+  float xsum[2][2][128];  // [item parity][half][key row]
   uint32_t tmem;
 };
 
-static_assert(sizeof(ColBars) <= 2048, "ColBars must fit the space reserved in ColCfg::SMEM");
+static_assert(sizeof(ColBars) <= 4096, "ColBars must fit the space reserved in ColCfg::SMEM");
 
 struct ColParams {
   const float* lse2;
@@ -436,29 +543,39 @@ struct ColParams {
 
 // Persistent like the forward kernel; items are (row, key tile), key tile 0
 // (the most query tiles) first. g counts query tiles so far, j items so far.
+// The key tile of an item is the A operand of all its MMAs, so it is read out
+// of shared memory once and kept in TMEM: the softmax warps copy the key tile
+// of item j + 1 into TMEM when they start item j (item j - 1's MMAs, the last
+// readers of that TMEM buffer, have completed by then).
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kColThreads, 1)
     attn_colsum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const ColParams p) {
   using C = ColCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sK = smem;
-  uint8_t* sQ = smem + C::TILE;
-  float* sL = reinterpret_cast<float*>(smem + (1 + C::QST) * C::TILE);
-  ColBars* bars = reinterpret_cast<ColBars*>(smem + (1 + C::QST) * C::TILE + C::QST * BM * 4);
+  uint8_t* sQ = smem + C::KST * C::TILE;
+  float* sL = reinterpret_cast<float*>(smem + (C::KST + C::QST) * C::TILE);
+  ColBars* bars = reinterpret_cast<ColBars*>(smem + (C::KST + C::QST) * C::TILE + C::LST * BM * 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = blockIdx.x < p.items ? (p.items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->k_full, 1);
-    mbar_init(&bars->k_empty, 1);
-    for (int i = 0; i < C::QST; ++i) {
-      mbar_init(&bars->q_full[i], 1);
-      mbar_init(&bars->q_empty[i], 1 + 8);  // MMA commit + one arrival per softmax warp
-    }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 8);  // one arrival per softmax warp after its copy
+      mbar_init(&bars->ka_full[i], 8);
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->s_free[i], 8);
+    }
+    for (int i = 0; i < C::QST; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+    }
+    for (int i = 0; i < C::LST; ++i) {
+      mbar_init(&bars->l_full[i], 1);
+      mbar_init(&bars->l_empty[i], 8);
     }
     for (int i = 0; i < 4; ++i) mbar_init(&bars->ebar[i], 2);
     fence_barrier_init();
@@ -477,41 +594,58 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem;
 
   if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    // Key tiles run two items ahead: items 0 and 1 first, then the key tile of
+    // item j + 2 once the query tiles of item j are issued.
     if (lane == 0) {
-      uint32_t g = 0;
-      bool ok = true;
-      int j = 0;
-      for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x, ++j) {
+      auto load_k = [&](int n) -> bool {
         int row, kt;
-        item_coords(it, p.rows, p.nqt, p.rb, row, kt);
+        item_coords(blockIdx.x + n * gridDim.x, p.rows, p.nqt, p.rb, row, kt);
+        const int ks = n & 1;
+        if (n >= 2 && !mbar_wait(&bars->k_empty[ks], ((n >> 1) - 1) & 1, p.err)) return false;
+        mbar_arrive_expect_tx(&bars->k_full[ks], C::TILE);
+        load_tile<D>(sK + ks * C::TILE, &tk, kt, row, &bars->k_full[ks]);
+        return true;
+      };
+      bool ok = true;
+      for (int n = 0; ok && n < min(2, n_items); ++n) ok = load_k(n);
+      uint32_t g = 0;
+      for (int j = 0; ok && j < n_items; ++j) {
+        int row, kt;
+        item_coords(blockIdx.x + j * gridDim.x, p.rows, p.nqt, p.rb, row, kt);
         const int nq = p.nqt - kt;
-        if (j > 0 && !mbar_wait(&bars->k_empty, (j - 1) & 1, p.err)) break;
-        mbar_arrive_expect_tx(&bars->k_full, C::TILE);
-        load_tile<D>(sK, &tk, kt, row, &bars->k_full);
         for (int i = 0; i < nq; ++i, ++g) {
-          const int st = g % C::QST, qt = kt + i;
+          const int st = g % C::QST, ls = g % C::LST, qt = kt + i;
           if (g >= C::QST && !mbar_wait(&bars->q_empty[st], ((g / C::QST) - 1) & 1, p.err)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bars->q_full[st], C::TILE + BM * 4);
+          mbar_arrive_expect_tx(&bars->q_full[st], C::TILE);
           load_tile<D>(sQ + st * C::TILE, &tq, qt, row, &bars->q_full[st]);
-          bulk_copy_g2s(sL + st * BM, p.lse2 + static_cast<size_t>(row) * p.Tp + qt * BM, BM * 4,
-                        &bars->q_full[st]);
+          if (g >= C::LST && !mbar_wait(&bars->l_empty[ls], ((g / C::LST) - 1) & 1, p.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->l_full[ls], BM * 4);
+          bulk_copy_g2s(sL + ls * BM, p.lse2 + static_cast<size_t>(row) * p.Tp + qt * BM, BM * 4,
+                        &bars->l_full[ls]);
         }
+        if (ok && j + 2 < n_items) ok = load_k(j + 2);
       }
     }
   } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    // S^T = K Q^T with K from TMEM (A) and the query tile from shared memory (B).
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(BN, BM, 0, 0);  // M = keys, N = queries
       uint32_t g = 0;
-      bool ok = true;
-      int j = 0;
-      for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x, ++j) {
+      for (int j = 0; j < n_items; ++j) {
         int row, kt;
-        item_coords(it, p.rows, p.nqt, p.rb, row, kt);
+        item_coords(blockIdx.x + j * gridDim.x, p.rows, p.nqt, p.rb, row, kt);
         const int nq = p.nqt - kt;
-        if (!mbar_wait(&bars->k_full, j & 1, p.err)) break;
+        const int kb = j & 1;
+        if (!mbar_wait(&bars->ka_full[kb], (j >> 1) & 1, p.err)) break;
+        bool ok = true;
         for (int i = 0; i < nq; ++i) {
           const uint32_t gq = g + i;
           const int st = gq % C::QST, sb = gq & 1;
@@ -524,12 +658,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint8_t* q_tile = sQ + st * C::TILE;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + sb * 128, desc_kmajor<D>(sK, kk), desc_kmajor<D>(q_tile, kk), idesc,
-                    kk > 0);
+            umma_ts(tmem + sb * 128, tmem + C::KA_COL + kb * (D / 2) + kk * 8,
+                    desc_kmajor<D>(q_tile, kk), idesc, kk > 0);
           umma_commit(&bars->s_full[sb]);
           umma_commit(&bars->q_empty[st]);
         }
-        umma_commit(&bars->k_empty);
+        if (!ok) break;
         g += nq;
       }
     }
@@ -542,17 +676,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quad * 32 + lane;  // key row within the tile
     const int cb = half * 64;        // first query column of this half
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    // Copies this thread's key row, this warp's half of the channels (D/4
+    // bf16 pairs), from the staged key tile into TMEM buffer n & 1.
+    auto copy_k = [&](int n) -> bool {
+      const int ks = n & 1;
+      if (!warp_wait(&bars->k_full[ks], (n >> 1) & 1, p.err)) return false;
+      const uint8_t* tile = sK + ks * C::TILE;
+      uint32_t w[D / 4];
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {  // 16-byte chunks of 8 channels
+        const int cg = half * (D / 16) + c;
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + (cg >> 3) * kBoxBytes + r * 128 +
+                                                        (((cg & 7) ^ (r & 7)) << 4));
+        w[4 * c] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+      }
+      const uint32_t dst = tmem + lane_off + C::KA_COL + (n & 1) * (D / 2) + half * (D / 4);
+      if constexpr (D == 128)
+        tmem_st32(dst, w);
+      else
+        tmem_st16(dst, w);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars->ka_full[n & 1]);
+        mbar_arrive(&bars->k_empty[ks]);
+      }
+      return true;
+    };
     uint32_t g = 0;
-    bool ok = true;
-    int j = 0;
-    for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x, ++j) {
+    bool ok = n_items == 0 || copy_k(0);
+    for (int j = 0; ok && j < n_items; ++j) {
       int row, kt;
-      item_coords(it, p.rows, p.nqt, p.rb, row, kt);
+      item_coords(blockIdx.x + j * gridDim.x, p.rows, p.nqt, p.rb, row, kt);
       const int nq = p.nqt - kt;
+      if (j + 1 < n_items && !copy_k(j + 1)) break;
       float acc = 0.f;
       for (int i = 0; i < nq; ++i) {
         const uint32_t gq = g + i;
-        const int st = gq % C::QST, sb = gq & 1, qt = kt + i;
+        const int ls = gq % C::LST, sb = gq & 1, qt = kt + i;
         if (!warp_wait(&bars->s_full[sb], (gq >> 1) & 1, p.err)) {
           ok = false;
           break;
@@ -565,11 +730,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_free[sb]);
-        if (!warp_wait(&bars->q_full[st], (gq / C::QST) & 1, p.err)) {
+        if (!warp_wait(&bars->l_full[ls], (gq / C::LST) & 1, p.err)) {
           ok = false;
           break;
         }
-        const float* L = sL + st * BM + cb;
+        const float* L = sL + ls * BM + cb;
         const int qvalid = min(BM, p.T - qt * BM) - cb;  // queries past the prompt end are padding
         // Eight independent sums; the LSE values come as float4 loads.
         float a8[8];
@@ -602,17 +767,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         acc += ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->q_empty[st]);
+        if (lane == 0) mbar_arrive(&bars->l_empty[ls]);
       }
       if (!ok) break;
       // add the two halves
-      bars->xsum[half][r] = acc;
+      bars->xsum[j & 1][half][r] = acc;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->ebar[quad]);
       if (!warp_wait(&bars->ebar[quad], j & 1, p.err)) break;
       const int key = kt * BN + r;
       if (half == 0 && key < p.T)
-        p.colsum[static_cast<size_t>(row) * p.T + key] = acc + bars->xsum[1][r];
+        p.colsum[static_cast<size_t>(row) * p.T + key] = acc + bars->xsum[j & 1][1][r];
       g += nq;
     }
   }
@@ -671,14 +836,32 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int rows, int T, int D) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Output [rows, T, D] fp32 as the target of the epilogue's TMA stores: boxes
+// of 32 tokens x 32 channels (128 bytes, 128-byte swizzle); tokens past T are
+// clipped, so the last tile of a row never writes into the next row.
+cudaError_t make_store_map(CUtensorMap* m, void* base, int rows, int T, int D) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(T) * D * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int D>
 cudaError_t forward_t(const void* Q, const void* K, const void* V, int rows, int T, float* O,
                       float* lse2, int32_t* err, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   cudaError_t e;
   if ((e = make_map(&mq, Q, rows, T, D)) != cudaSuccess) return e;
   if ((e = make_map(&mk, K, rows, T, D)) != cudaSuccess) return e;
   if ((e = make_map(&mv, V, rows, T, D)) != cudaSuccess) return e;
+  if ((e = make_store_map(&mo, O, rows, T, D)) != cudaSuccess) return e;
   static bool attr = false;
   if (!attr) {
     e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -687,10 +870,10 @@ cudaError_t forward_t(const void* Q, const void* K, const void* V, int rows, int
     attr = true;
   }
   const int nqt = (T + BM - 1) / BM;
-  FwdParams p{O, lse2, rows, T, lse_stride(T), nqt, rows * nqt, rows_per_l2_block(T, D, 2),
+  FwdParams p{lse2, rows, T, lse_stride(T), nqt, rows * nqt, rows_per_l2_block(T, D, 2),
               kLog2e / sqrtf(float(D)), err};
   const unsigned grid = static_cast<unsigned>(std::min(p.items, num_sms()));
-  attn_fwd_kernel<D><<<grid, kThreads, FwdCfg<D>::SMEM, stream>>>(mq, mk, mv, p);
+  attn_fwd_kernel<D><<<grid, kFwdThreads, FwdCfg<D>::SMEM, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
 
@@ -712,7 +895,7 @@ cudaError_t colsum_t(const void* Q, const void* K, const float* lse2, int rows, 
   ColParams p{lse2, colsum, rows, T, lse_stride(T), nqt, rows * nqt, rows_per_l2_block(T, D, 1),
               kLog2e / sqrtf(float(D)), err};
   const unsigned grid = static_cast<unsigned>(std::min(p.items, num_sms()));
-  attn_colsum_kernel<D><<<grid, kThreads, ColCfg<D>::SMEM, stream>>>(mq, mk, p);
+  attn_colsum_kernel<D><<<grid, kColThreads, ColCfg<D>::SMEM, stream>>>(mq, mk, p);
   return cudaGetLastError();
 }
 
