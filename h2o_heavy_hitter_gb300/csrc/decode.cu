@@ -74,10 +74,11 @@ struct DecodeShared {
   static constexpr int LPS = D / 8;   // lanes per slot (16 bytes each)
   static constexpr int G = NT / LPS;  // slot groups per CTA
   static constexpr int NW = NT / 32;
-  float red_ml[G][2];
-  float red_o[G][D];  // element i of lane l of group g at [g][i * LPS + l]
+  float red_ml[NW][2];
+  float red_o[NW][D];  // element i of lane l of warp w's merged group at [w][i * LPS + l]
+  float vnew[D];       // the new token's value vector
   float seg_w[kMaxDecodeSegs];
-  float part_m, part_l;
+  float s_new;
   float M, invL, w_new, p_new;
   unsigned long long wkey[NW];
   int wslot[NW];
@@ -114,6 +115,10 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
     const size_t off = static_cast<size_t>(row) * D + l * 8;
     knew = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.k_new) + off);
     vnew = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.v_new) + off);
+    float vf[8];
+    bf16x8_to_f32(vnew, vf);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sm.vnew[l * 8 + i] = vf[i];
   }
   grid_dependency_wait();  // the cache, scores and metadata are written by the previous step
 
@@ -216,42 +221,68 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   }
   grid_launch_dependents();
 
-  // ---- this CTA's partial: combine the groups.
-  if (l == 0) {
-    sm.red_ml[g][0] = m;
-    sm.red_ml[g][1] = lsum;
+  // ---- this CTA's partial. The groups of a warp are merged with shuffles,
+  // so shared memory holds one (max, sum, output) per warp. A group that saw
+  // no filled slot has m = -inf and undefined sums: it contributes nothing.
+  if (m == -INFINITY) {
+    lsum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = 0.f;
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) sm.red_o[g][i * LPS + l] = o[i];
-  __syncthreads();
-  float oc = 0.f;  // output element `tid` (tid < D) of this CTA, scaled to part_m
-  if (tid < D) {
-    const int gi = (tid % 8) * LPS + tid / 8;  // dim tid = lane (tid / 8), element tid % 8
-    float mc = -INFINITY;
-    for (int gg = 0; gg < G; ++gg) mc = fmaxf(mc, sm.red_ml[gg][0]);
-    float lc = 0.f;
-    for (int gg = 0; gg < G; ++gg) {
-      const float mg = sm.red_ml[gg][0];
-      if (mg != -INFINITY) {
-        const float w = ex2(mg - mc);
-        lc = fmaf(sm.red_ml[gg][1], w, lc);
-        oc = fmaf(sm.red_o[gg][gi], w, oc);
-      }
+  for (int off = LPS; off < 32; off <<= 1) {
+    const float mp = __shfl_xor_sync(0xffffffffu, m, off);
+    const float lp = __shfl_xor_sync(0xffffffffu, lsum, off);
+    const float mn = fmaxf(m, mp);
+    const float w = m == -INFINITY ? 0.f : ex2(m - mn);
+    const float wp = mp == -INFINITY ? 0.f : ex2(mp - mn);
+    lsum = lsum * w + lp * wp;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = o[i] * w + __shfl_xor_sync(0xffffffffu, o[i], off) * wp;
+    m = mn;
+  }
+  if (lane < LPS) {
+    if (lane == 0) {
+      sm.red_ml[warp][0] = m;
+      sm.red_ml[warp][1] = lsum;
     }
-    if (tid == 0) {
-      sm.part_m = mc;
-      sm.part_l = lc;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sm.red_o[warp][i * LPS + lane] = o[i];
+  }
+  if (g == 0) {  // logit of the new token (group 0 holds k_new)
+    float sn = dot8(knew, qf);
+#pragma unroll
+    for (int off = LPS / 2; off > 0; off >>= 1) sn += __shfl_xor_sync(gmask, sn, off);
+    if (l == 0) sm.s_new = sn;
+  }
+  __syncthreads();
+  // Every thread merges the warps' partials (max mc, sum lc); threads tid < D
+  // also their output element oc, scaled to mc.
+  float mc = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) mc = fmaxf(mc, sm.red_ml[w][0]);
+  float lc = 0.f, oc = 0.f;
+  const int gi = ((tid & (D - 1)) % 8) * LPS + (tid & (D - 1)) / 8;  // element tid % 8 of lane tid / 8
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    const float mg = sm.red_ml[w][0];
+    if (mg != -INFINITY) {
+      const float wt = ex2(mg - mc);
+      lc = fmaf(sm.red_ml[w][1], wt, lc);
+      if (tid < D) oc = fmaf(sm.red_o[w][gi], wt, oc);
     }
   }
+  const float s_new = sm.s_new;
 
-  // ---- hand the partial to the row's last CTA.
+  // ---- exact normaliser over the row and the new token.
+  float M, invL, w_new, p_new, w_self = 0.f;
   if (a.segs > 1) {
+    // hand the partial to the row's last CTA
     float* part = a.partial + (static_cast<size_t>(row) * a.segs + seg) * PS;
     if (tid < D) part[4 + tid] = oc;
-    __syncthreads();
     if (tid == 0) {
-      part[0] = sm.part_m;
-      part[1] = sm.part_l;
+      part[0] = mc;
+      part[1] = lc;
     }
     __threadfence();  // logits and partial visible before the arrival is counted
     __syncthreads();
@@ -259,43 +290,35 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
     __syncthreads();
     if (!sm.is_last) return;
     __threadfence();  // every other segment's writes are visible from here on
-  } else {
-    __syncthreads();
-  }
-
-  // ---- finish the row: exact normaliser, output, scores, eviction, slot write.
-  float s_new = 0.f;  // logit of the new token (group 0 holds k_new)
-  if (g == 0) {
-    s_new = dot8(knew, qf);
-#pragma unroll
-    for (int off = LPS / 2; off > 0; off >>= 1) s_new += __shfl_xor_sync(gmask, s_new, off);
-  }
-  if (tid == 0) {
-    float M = s_new, L;
-    if (a.segs > 1) {
+    if (tid == 0) {
+      float Mx = s_new;
       for (int c = 0; c < a.segs; ++c)
-        M = fmaxf(M, __ldcg(a.partial + (static_cast<size_t>(row) * a.segs + c) * PS));
-      L = ex2(s_new - M);
+        Mx = fmaxf(Mx, __ldcg(a.partial + (static_cast<size_t>(row) * a.segs + c) * PS));
+      float L = ex2(s_new - Mx);
       for (int c = 0; c < a.segs; ++c) {
         const float* pc = a.partial + (static_cast<size_t>(row) * a.segs + c) * PS;
-        const float mc = __ldcg(pc);
-        const float w = mc == -INFINITY ? 0.f : ex2(mc - M);
+        const float mcs = __ldcg(pc);
+        const float w = mcs == -INFINITY ? 0.f : ex2(mcs - Mx);
         sm.seg_w[c] = w;
         L = fmaf(__ldcg(pc + 1), w, L);
       }
-    } else {
-      M = fmaxf(M, sm.part_m);
-      const float w = sm.part_m == -INFINITY ? 0.f : ex2(sm.part_m - M);
-      sm.seg_w[0] = w;
-      L = fmaf(sm.part_l, w, ex2(s_new - M));
+      sm.M = Mx;
+      sm.invL = 1.f / L;
+      sm.w_new = ex2(s_new - Mx);
+      sm.p_new = sm.w_new * sm.invL;
     }
-    sm.M = M;
-    sm.invL = 1.f / L;
-    sm.w_new = ex2(s_new - M);
-    sm.p_new = sm.w_new * sm.invL;
+    __syncthreads();
+    M = sm.M;
+    invL = sm.invL;
+    w_new = sm.w_new;
+    p_new = sm.p_new;
+  } else {  // one CTA holds the whole row: every thread finishes from its own registers
+    M = fmaxf(s_new, mc);
+    w_self = mc == -INFINITY ? 0.f : ex2(mc - M);
+    w_new = ex2(s_new - M);
+    invL = 1.f / fmaf(lc, w_self, w_new);
+    p_new = w_new * invL;
   }
-  __syncthreads();
-  const float M = sm.M, invL = sm.invL, p_new = sm.p_new;
   if (tid < D) {
     float acc = 0.f;
     if (a.segs > 1) {
@@ -303,11 +326,9 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
         acc = fmaf(__ldcg(a.partial + (static_cast<size_t>(row) * a.segs + c) * PS + 4 + tid),
                    sm.seg_w[c], acc);
     } else {
-      acc = oc * sm.seg_w[0];
+      acc = oc * w_self;
     }
-    const float vn = __bfloat162float(
-        static_cast<const __nv_bfloat16*>(a.v_new)[static_cast<size_t>(row) * D + tid]);
-    a.out[static_cast<size_t>(row) * D + tid] = fmaf(vn, sm.w_new, acc) * invL;
+    a.out[static_cast<size_t>(row) * D + tid] = fmaf(sm.vnew[tid], w_new, acc) * invL;
   }
 
   // Scores of every occupied slot of the row; this CTA's smallest candidate key.

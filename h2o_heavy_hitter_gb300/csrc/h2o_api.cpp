@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdint>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -86,6 +87,13 @@ struct h2o_ctx {
 namespace {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Prompt tensors and prefill outputs are read and written by TMA, which needs
+// 16-byte aligned addresses.
+bool tma_aligned(const void* a, const void* b, const void* c, const void* d) {
+  auto ok = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
+  return ok(a) && ok(b) && ok(c) && ok(d);
+}
 
 int check_layer(const h2o_ctx* c, int layer) {
   if (!c) return fail(H2O_EINVAL, "null context");
@@ -217,6 +225,7 @@ int h2o_prefill(h2o_ctx* c, int layer, const void* Q, const void* K, const void*
     return H2O_OK;
   }
   if (!Q || !K || !V || !out) return fail(H2O_EINVAL, "null Q, K, V or out");
+  if (!tma_aligned(Q, K, V, out)) return fail(H2O_EINVAL, "Q, K, V and out must be 16-byte aligned");
   try {
     Scratch colsum(static_cast<size_t>(c->rows) * T * sizeof(float), s);
     int rc = run_attention(Q, K, V, c->rows, T, c->d, out, static_cast<float*>(colsum.p), c->err, s);
@@ -240,6 +249,7 @@ int h2o_prefill_attention(const void* Q, const void* K, const void* V, int rows,
   if (head_dim != 64 && head_dim != 128) return fail(H2O_EINVAL, "head_dim must be 64 or 128");
   if (static_cast<long>(rows) * T == 0) return H2O_OK;
   if (!Q || !K || !V || !out || !score) return fail(H2O_EINVAL, "null pointer");
+  if (!tma_aligned(Q, K, V, out)) return fail(H2O_EINVAL, "Q, K, V and out must be 16-byte aligned");
   try {
     return run_attention(Q, K, V, rows, T, head_dim, out, score, nullptr, current_stream());
   } catch (const std::exception& ex) {
@@ -258,6 +268,7 @@ int h2o_prefill_attention_noalloc(const void* Q, const void* K, const void* V, i
                                 std::to_string(H2O_NOALLOC_MAX_LSE) + " floats");
   if (need == 0) return H2O_OK;
   if (!Q || !K || !V || !out || !score) return fail(H2O_EINVAL, "null pointer");
+  if (!tma_aligned(Q, K, V, out)) return fail(H2O_EINVAL, "Q, K, V and out must be 16-byte aligned");
   float* lse = nullptr;
   cudaError_t e = h2o::noalloc_lse_scratch(&lse);
   if (e != cudaSuccess) return cuda_fail(e, "scratch address lookup");

@@ -4,16 +4,17 @@
 // summary page, section 3.2 and appendix A, Pseudocode).
 //
 // Two passes over the causal (query, key) tile pairs, 128 x 128 tiles:
-//   forward: one item per (row, query tile). S = Q K^T in TMEM (tcgen05.mma, bf16
-//            operands staged by TMA with 128-byte swizzle), online softmax in
-//            registers (one thread per query row and half of the keys,
-//            base-2 logits), P written back as bf16 over the S columns it came
-//            from, and O += P V issued with P as the TMEM operand. The running
-//            max is only raised when it grows by more than 2^8, so O is rarely
-//            rescaled. O is double-buffered in TMEM by item, so dedicated
-//            epilogue warps normalise and store item j (TMA stores through a
-//            small staging tile) while item j + 1 runs. Writes O (fp32) and
-//            the base-2 log-sum-exp of every query row.
+//   forward: one item per (row, block of two query tiles A and B). Every K/V
+//            tile loaded serves both query tiles. S_t = Q_t K^T in TMEM
+//            (tcgen05.mma, bf16 operands staged by TMA with 128-byte swizzle),
+//            online softmax in registers (one thread per query row, base-2
+//            logits), P written back as bf16 over the S columns it came from,
+//            and O_t += P_t V issued with P as the TMEM operand; the softmax of
+//            one tile overlaps the MMAs of the other. The running max is only
+//            raised when it grows by more than 2^8, so O is rarely rescaled.
+//            The softmax warps read the finished O out of TMEM, release it,
+//            and write it normalised with TMA stores through small staging
+//            tiles. Writes O (fp32) and the base-2 log-sum-exp of every query.
 //   colsum:  one item per (row, key tile). S^T = K Q^T in TMEM (one thread per
 //            key row) with the key tile held in TMEM as the A operand, so each
 //            MMA reads only the query tile from shared memory; P = 2^(s - lse2)
@@ -24,9 +25,10 @@
 //
 // Both kernels are persistent (one CTA per SM walking a longest-first item
 // list) and warp-specialised: TMA producer warps, one MMA warp that owns the
-// TMEM, softmax warps (two per TMEM lane quadrant) and, in the forward pass,
-// epilogue warps. Every mbarrier wait is bounded; a wait that gives up sets
-// the device error word and the CTA unwinds, always freeing its Tensor Memory.
+// TMEM, and softmax warps (one per TMEM lane quadrant and query tile in the
+// forward pass, two per lane quadrant in the column sums). Every mbarrier wait
+// is bounded; a wait that gives up sets the device error word and the CTA
+// unwinds, always freeing its Tensor Memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -57,9 +59,9 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// The shared-memory source of every committed store has been read.
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// At most one committed store has not yet read its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // Every committed store has completed.
 __device__ __forceinline__ void bulk_wait_all() {
@@ -71,53 +73,48 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ------------------------------------------------------------------ forward
-// Warp roles of the forward kernel (15 warps).
+// An item of the forward kernel is a block of 256 query rows of one row:
+// query tiles A = 2 qb and B = 2 qb + 1. Every K/V tile loaded serves both
+// query tiles, which halves the K/V traffic out of L2 per flop.
+// Warp roles (11 warps):
 constexpr int kWarpQK = 0;        // TMA loads of Q and K
 constexpr int kWarpMMA = 1;       // owns TMEM, issues every tcgen05.mma
-constexpr int kWarpSoftmax0 = 2;  // warps 2..9: softmax, two per TMEM lane quadrant
-constexpr int kWarpEpi0 = 10;     // warps 10..13: epilogue, one per lane quadrant
-constexpr int kWarpV = 14;        // TMA loads of V
-constexpr int kFwdThreads = 15 * 32;
-constexpr int kSoftmaxThreads = 256;
-constexpr int kEpiWarps = 4;
+constexpr int kWarpV = 2;         // TMA loads of V
+constexpr int kWarpSoftmax0 = 3;  // warps 3..6: tile A, 7..10: tile B, one per TMEM lane quadrant
+constexpr int kFwdThreads = 11 * 32;
+constexpr int kTileThreads = 128;  // softmax threads of one query tile (one per query row)
 
 template <int D>
 struct FwdCfg {
-  static constexpr int KST = D == 128 ? 3 : 4;  // K tiles in flight
+  static constexpr int KST = D == 128 ? 2 : 3;  // K tiles in flight
   static constexpr int VST = D == 128 ? 2 : 3;  // V tiles in flight
   static constexpr int TILE = BM * D * 2;
-  // TMEM: S buffers b = 0, 1 at columns [128 b, 128 b + 128); the bf16 P of a
-  // tile overwrites its own S buffer (keys [64 h, 64 h + 64) at columns
-  // 64 h + [0, 32)); O buffers by item parity at 256 + 128 b.
-  static constexpr uint32_t S_COL = 0;
+  // TMEM: S of tile t at columns [128 t, 128 t + 128); the bf16 P of a tile
+  // overwrites its own S (keys [16 i, 16 i + 16) at columns [8 i, 8 i + 8));
+  // O of tile t at 256 + 128 t.
   static constexpr uint32_t O_COL = 256;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr int STAGE_BYTES = 32 * 32 * 4;  // epilogue staging per warp: 32 rows x 32 fp32
-  static constexpr size_t TILES = static_cast<size_t>(1 + KST + VST) * TILE;
-  static constexpr size_t SMEM = TILES + kEpiWarps * STAGE_BYTES + 1024 + 6144;
+  static constexpr int STAGE_BYTES = 32 * 16 * 4;  // one staging tile: 32 rows x 16 fp32
+  static constexpr size_t TILES = static_cast<size_t>(2 + KST + VST) * TILE;
+  // two staging tiles per softmax warp; barriers; slack for 1024-byte alignment
+  static constexpr size_t SMEM = TILES + 8 * 2 * STAGE_BYTES + 1024 + 2048;
 };
 
 struct FwdBars {
   uint64_t q_full, q_empty;
   uint64_t k_full[4], k_empty[4];
   uint64_t v_full[4], v_empty[4];
-  uint64_t s_full[2], p_ready[2];
-  uint64_t o_done;      // one phase per PV (waited only by the rare O rescale)
-  uint64_t o_last[2];   // per O buffer, one phase per item: the item's last PV completed
-  uint64_t o_free[2];   // per O buffer, one phase per item: the epilogue read O out of TMEM
-  uint64_t l_ready[2];  // per O buffer, one phase per item: row sums and maxima posted
-  uint64_t xbar[4];     // per lane quadrant, one phase per tile: both halves' maxima posted
-  float xmax[2][2][128];  // [tile parity][half][row]
-  float lsum[2][2][128];  // [O buffer][half][row]: the half's row sum
-  float lmax[2][128];     // [O buffer][row]: the row's final running max (base-2 units)
+  uint64_t s_full[2], p_ready[2];  // per query tile, one phase per key tile
+  uint64_t o_last[2];  // per query tile, one phase per item: the tile's last PV completed
+  uint64_t o_free[2];  // per query tile, one phase per item: its O has been read out of TMEM
   uint32_t tmem;
 };
 
-static_assert(sizeof(FwdBars) <= 6144, "FwdBars must fit the space reserved in FwdCfg::SMEM");
+static_assert(sizeof(FwdBars) <= 2048, "FwdBars must fit the space reserved in FwdCfg::SMEM");
 
 struct FwdParams {
   float* lse2;
-  int rows, T, Tp, nqt, items;
+  int rows, T, Tp, nqt, nqb, items;  // nqb = blocks of two query tiles per row
   int rb;  // rows per L2 block of the item order
   float qscale;
   int32_t* err;
@@ -164,11 +161,16 @@ __device__ __forceinline__ uint64_t desc_kmajor(const uint8_t* tile, int kk) {
   return smem_desc(tile + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
 }
 
-// Persistent: CTA b takes work items b, b + grid, ... of a list ordered by
-// decreasing work (query tile nqt-1 of every row first). Barrier phases run on
-// per-CTA counters that every role advances identically: g = K/V tiles so far,
-// j = items so far. Item j accumulates into O buffer j & 1, so the epilogue
-// warps read item j out of TMEM while item j + 1 already runs.
+// Persistent: CTA b takes items b, b + grid, ... of a list ordered by
+// decreasing work (the last query block of every row first). Barrier phases
+// run on per-CTA counters that every role advances identically: g = K/V tiles
+// so far, n[t] = key tiles processed by query tile t so far, e[t] = items in
+// which tile t took part. The MMA issue order per key tile kt is
+//   PV_A(kt-1), S_A(kt), PV_B(kt-1), S_B(kt),
+// so the softmax of one tile overlaps the two MMAs of the other, and S_t(kt)
+// (which overwrites P_t(kt-1)) follows the PV that reads it. The MMAs of one
+// thread run in issue order; when the softmax sees S_t(kt) complete, every PV
+// of tile t before it has completed too, so O_t can be rescaled right away.
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -177,11 +179,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* sQ = smem;
-  uint8_t* sK = smem + C::TILE;
-  uint8_t* sV = smem + (1 + C::KST) * C::TILE;
+  uint8_t* sQ = smem;  // tile A, then tile B
+  uint8_t* sK = smem + 2 * C::TILE;
+  uint8_t* sV = smem + (2 + C::KST) * C::TILE;
   uint8_t* sStage = smem + C::TILES;
-  FwdBars* bars = reinterpret_cast<FwdBars*>(sStage + kEpiWarps * C::STAGE_BYTES);
+  FwdBars* bars = reinterpret_cast<FwdBars*>(sStage + 16 * C::STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -195,15 +197,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_ready[i], kSoftmaxThreads);
-      mbar_init(&bars->o_last[i], 1);
-      mbar_init(&bars->o_free[i], kEpiWarps);
-      mbar_init(&bars->l_ready[i], kSoftmaxThreads / 32);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_ready[t], kTileThreads);
+      mbar_init(&bars->o_last[t], 1);
+      mbar_init(&bars->o_free[t], kTileThreads / 32);
     }
-    mbar_init(&bars->o_done, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&bars->xbar[i], 2);
     fence_barrier_init();
   }
   if (warp == kWarpMMA) {
@@ -213,56 +212,49 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == kWarpQK && lane == 0) {
     tma_prefetch_map(&tq);
     tma_prefetch_map(&tk);
-    tma_prefetch_map(&to);
   }
   if (warp == kWarpV && lane == 0) tma_prefetch_map(&tv);
+  if (warp == kWarpSoftmax0 && lane == 0) tma_prefetch_map(&to);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
 
-  if (warp == kWarpQK) {
-    // ---------------------------------------------------------------- TMA: Q and K
+  if (warp == kWarpQK || warp == kWarpV) {
+    // ---------------------------------------------------------------- TMA loads
+    // Warp 0 loads the item's query tiles and its K tiles, warp 2 its V tiles,
+    // so K tiles are never held back by a wait for a V stage.
     if (lane == 0) {
+      const bool is_k = warp == kWarpQK;
+      const int nst = is_k ? C::KST : C::VST;
+      uint64_t* full = is_k ? bars->k_full : bars->v_full;
+      uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+      uint8_t* ring = is_k ? sK : sV;
+      const CUtensorMap* map = is_k ? &tk : &tv;
       uint32_t g = 0;
       bool ok = true;
       int j = 0;
       for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x, ++j) {
         int row, rank;
-        item_coords(it, p.rows, p.nqt, p.rb, row, rank);
-        const int qt = p.nqt - 1 - rank;
-        if (j > 0 && !mbar_wait(&bars->q_empty, (j - 1) & 1, p.err)) break;  // last QK^T done
-        mbar_arrive_expect_tx(&bars->q_full, C::TILE);
-        load_tile<D>(sQ, &tq, qt, row, &bars->q_full);
-        for (int kt = 0; kt <= qt; ++kt, ++g) {
-          const int ks = g % C::KST;
-          if (g >= C::KST && !mbar_wait(&bars->k_empty[ks], ((g / C::KST) - 1) & 1, p.err)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&bars->k_full[ks], C::TILE);
-          load_tile<D>(sK + ks * C::TILE, &tk, kt, row, &bars->k_full[ks]);
+        item_coords(it, p.rows, p.nqb, p.rb, row, rank);
+        const int qa = 2 * (p.nqb - 1 - rank);
+        const bool has_b = qa + 1 < p.nqt;
+        const int nk = has_b ? qa + 2 : qa + 1;
+        if (is_k) {
+          if (j > 0 && !mbar_wait(&bars->q_empty, (j - 1) & 1, p.err)) break;  // last S done
+          mbar_arrive_expect_tx(&bars->q_full, (has_b ? 2 : 1) * C::TILE);
+          load_tile<D>(sQ, &tq, qa, row, &bars->q_full);
+          if (has_b) load_tile<D>(sQ + C::TILE, &tq, qa + 1, row, &bars->q_full);
         }
-      }
-    }
-  } else if (warp == kWarpV) {
-    // ---------------------------------------------------------------- TMA: V
-    // Its own warp, so K tiles are never held back by a wait for a V stage.
-    if (lane == 0) {
-      uint32_t g = 0;
-      bool ok = true;
-      for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x) {
-        int row, rank;
-        item_coords(it, p.rows, p.nqt, p.rb, row, rank);
-        const int qt = p.nqt - 1 - rank;
-        for (int kt = 0; kt <= qt; ++kt, ++g) {
-          const int vs = g % C::VST;
-          if (g >= C::VST && !mbar_wait(&bars->v_empty[vs], ((g / C::VST) - 1) & 1, p.err)) {
+        for (int kt = 0; kt < nk; ++kt, ++g) {
+          const int st = g % nst;
+          if (g >= static_cast<uint32_t>(nst) &&
+              !mbar_wait(&empty[st], ((g / nst) - 1) & 1, p.err)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bars->v_full[vs], C::TILE);
-          load_tile<D>(sV + vs * C::TILE, &tv, kt, row, &bars->v_full[vs]);
+          mbar_arrive_expect_tx(&full[st], C::TILE);
+          load_tile<D>(ring + st * C::TILE, map, kt, row, &full[st]);
         }
       }
     }
@@ -271,118 +263,144 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(BM, D, 0, 1);
-      uint32_t g = 0;
+      uint32_t g = 0, n0 = 0, n1 = 0, e1 = 0;
       bool ok = true;
       int j = 0;
+      auto pv = [&](int t, uint32_t gp, bool first) {
+        const uint8_t* v_tile = sV + (gp % C::VST) * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          // B = V tile, MN-major: 16 keys = two 8-row swizzle atoms (2048 B);
+          // the two 64-column halves of d sit one TMA box (16 KB) apart.
+          const uint64_t bdesc = smem_desc(v_tile + kk * 2048, kBoxBytes, 1024);
+          umma_ts(tmem + C::O_COL + t * 128, tmem + t * 128 + kk * 8, bdesc, idesc_pv,
+                  (!first || kk > 0) ? 1u : 0u);
+        }
+      };
+      auto qk = [&](int t, uint32_t gk) {
+        const uint8_t* k_tile = sK + (gk % C::KST) * C::TILE;
+        const uint8_t* q_tile = sQ + t * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + t * 128, desc_kmajor<D>(q_tile, kk), desc_kmajor<D>(k_tile, kk),
+                  idesc_qk, kk > 0);
+      };
       for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x, ++j) {
         int row, rank;
-        item_coords(it, p.rows, p.nqt, p.rb, row, rank);
-        const int nkt = p.nqt - rank;
-        const int ob = j & 1;
+        item_coords(it, p.rows, p.nqb, p.rb, row, rank);
+        const int qa = 2 * (p.nqb - 1 - rank);
+        const bool has_b = qa + 1 < p.nqt;
+        const int nk = has_b ? qa + 2 : qa + 1;
+        const int last_a = qa, last_b = qa + 1;
         if (!mbar_wait(&bars->q_full, j & 1, p.err)) break;
-        for (int kt = 0; kt <= nkt; ++kt) {
-          if (kt < nkt) {
-            // S(gk) overwrites S/P(gk - 2), whose PV was issued before it:
-            // the MMAs of this thread run in issue order.
-            const uint32_t gk = g + kt;
-            const int ks = gk % C::KST, sb = gk & 1;
-            if (!mbar_wait(&bars->k_full[ks], (gk / C::KST) & 1, p.err)) {
+        for (int kt = 0; ok && kt <= nk; ++kt) {
+          const uint32_t gp = g + kt - 1, gk = g + kt;
+          bool v_ready = false, k_ready = false;
+          // ---- tile A: PV_A(kt - 1), then S_A(kt)
+          if (kt >= 1 && kt - 1 <= last_a) {
+            if (!mbar_wait(&bars->p_ready[0], (n0 + kt - 1) & 1, p.err) ||
+                !mbar_wait(&bars->v_full[gp % C::VST], (gp / C::VST) & 1, p.err) ||
+                (kt == 1 && j > 0 && !mbar_wait(&bars->o_free[0], (j - 1) & 1, p.err))) {
               ok = false;
               break;
             }
+            v_ready = true;
             tc_fence_after();
-            const uint8_t* k_tile = sK + ks * C::TILE;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              umma_ss(tmem + C::S_COL + sb * 128, desc_kmajor<D>(sQ, kk), desc_kmajor<D>(k_tile, kk),
-                      idesc_qk, kk > 0);
-            umma_commit(&bars->s_full[sb]);
-            umma_commit(&bars->k_empty[ks]);
-            if (kt == nkt - 1) umma_commit(&bars->q_empty);
+            pv(0, gp, kt == 1);
+            if (kt - 1 == last_a) umma_commit(&bars->o_last[0]);
+            if (!has_b) umma_commit(&bars->v_empty[gp % C::VST]);
           }
+          if (kt < nk && kt <= last_a) {
+            if (!mbar_wait(&bars->k_full[gk % C::KST], (gk / C::KST) & 1, p.err)) {
+              ok = false;
+              break;
+            }
+            k_ready = true;
+            tc_fence_after();
+            qk(0, gk);
+            umma_commit(&bars->s_full[0]);
+            if (!has_b) {
+              umma_commit(&bars->k_empty[gk % C::KST]);
+              if (kt == nk - 1) umma_commit(&bars->q_empty);
+            }
+          }
+          if (!has_b) continue;
+          // ---- tile B: PV_B(kt - 1), then S_B(kt)
           if (kt >= 1) {
-            const uint32_t gp = g + kt - 1;
-            const int pb = gp & 1, vs = gp % C::VST;
-            if (!mbar_wait(&bars->p_ready[pb], (gp >> 1) & 1, p.err) ||
-                !mbar_wait(&bars->v_full[vs], (gp / C::VST) & 1, p.err) ||
-                (kt == 1 && j >= 2 && !mbar_wait(&bars->o_free[ob], ((j >> 1) - 1) & 1, p.err))) {
+            if (!mbar_wait(&bars->p_ready[1], (n1 + kt - 1) & 1, p.err) ||
+                (!v_ready && !mbar_wait(&bars->v_full[gp % C::VST], (gp / C::VST) & 1, p.err)) ||
+                (kt == 1 && e1 > 0 && !mbar_wait(&bars->o_free[1], (e1 - 1) & 1, p.err))) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint8_t* v_tile = sV + vs * C::TILE;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              // B = V tile, MN-major: 16 keys = two 8-row swizzle atoms (2048 B);
-              // the two 64-column halves of d sit one TMA box (16 KB) apart.
-              const uint64_t bdesc = smem_desc(v_tile + kk * 2048, kBoxBytes, 1024);
-              const uint32_t a_tmem = tmem + C::S_COL + pb * 128 + (kk >> 2) * 64 + (kk & 3) * 8;
-              umma_ts(tmem + C::O_COL + ob * 128, a_tmem, bdesc, idesc_pv,
-                      (kt > 1 || kk > 0) ? 1u : 0u);
+            pv(1, gp, kt == 1);
+            umma_commit(&bars->v_empty[gp % C::VST]);
+            if (kt - 1 == last_b) umma_commit(&bars->o_last[1]);
+          }
+          if (kt < nk) {
+            if (!k_ready && !mbar_wait(&bars->k_full[gk % C::KST], (gk / C::KST) & 1, p.err)) {
+              ok = false;
+              break;
             }
-            umma_commit(&bars->v_empty[vs]);
-            umma_commit(&bars->o_done);
-            if (kt == nkt) umma_commit(&bars->o_last[ob]);
+            tc_fence_after();
+            qk(1, gk);
+            umma_commit(&bars->s_full[1]);
+            umma_commit(&bars->k_empty[gk % C::KST]);
+            if (kt == nk - 1) umma_commit(&bars->q_empty);
           }
         }
-        g += nkt;
+        g += nk;
+        n0 += last_a + 1;
+        if (has_b) {
+          n1 += last_b + 1;
+          ++e1;
+        }
       }
     }
-  } else if (warp < kWarpEpi0) {
-    // ---------------------------------------------------------------- softmax
-    // Two warps per TMEM lane quadrant, one per half of the 128 S columns; a
-    // thread owns one query row's half. The halves share the row's running max
-    // (tile maxima exchanged through shared memory every tile); at the end of
-    // an item each posts its row sum for the epilogue warps.
-    const int sw = warp - kWarpSoftmax0;
-    const int quad = warp & 3, half = sw >> 2;
+  } else {
+    // ---------------------------------------------------------------- softmax + epilogue
+    // Four warps per query tile, one per TMEM lane quadrant; a thread owns one
+    // query row and all 128 keys of each S tile.
+    const int sw = warp - kWarpSoftmax0;  // 0..7
+    const int t = sw >> 2;                // query tile: 0 = A, 1 = B
+    const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int cb = half * 64;  // first S column of this half
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    uint32_t g = 0;
+    const uint32_t s_tm = tmem + lane_off + t * 128;
+    const uint32_t o_tm = tmem + lane_off + C::O_COL + t * 128;
+    uint32_t n = 0, e = 0, rounds = 0;
     bool ok = true;
-    int j = 0;
-    for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x, ++j) {
+    for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x) {
       int row, rank;
-      item_coords(it, p.rows, p.nqt, p.rb, row, rank);
-      const int qt = p.nqt - 1 - rank;
-      const int nkt = qt + 1;
-      const int ob = j & 1;
+      item_coords(it, p.rows, p.nqb, p.rb, row, rank);
+      const int qt = 2 * (p.nqb - 1 - rank) + t;
+      if (qt >= p.nqt) continue;  // tile B of a ragged last block: nothing to do
+      const int qrow = qt * BM + r;
       float m = -INFINITY, l = 0.f;
-      for (int kt = 0; kt < nkt; ++kt) {
-        const uint32_t gs = g + kt;
-        const int sb = gs & 1;
-        const uint32_t s_tm = tmem + lane_off + C::S_COL + sb * 128;
-        if (!warp_wait(&bars->s_full[sb], (gs >> 1) & 1, p.err)) {
+      for (int kt = 0; kt <= qt; ++kt) {
+        if (!warp_wait(&bars->s_full[t], (n + kt) & 1, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t s[64];
-        tmem_ld32(s_tm + cb, s);
-        tmem_ld32(s_tm + cb + 32, s + 32);
+        uint32_t s[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + c * 32, s + c * 32);
         tmem_wait_ld();
         if (kt == qt) {  // diagonal tile: key c is visible to query r iff c <= r
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (cb + c > r) s[c] = __float_as_uint(-INFINITY);
+          for (int c = 0; c < 128; ++c)
+            if (c > r) s[c] = __float_as_uint(-INFINITY);
         }
         float mx8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = __uint_as_float(s[e]);
+        for (int x = 0; x < 8; ++x) mx8[x] = __uint_as_float(s[x]);
 #pragma unroll
-        for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(s[c]));
-        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        // exchange the half maxima of this row with the partner warp
-        bars->xmax[gs & 1][half][r] = mx;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->xbar[quad]);
-        if (!warp_wait(&bars->xbar[quad], gs & 1, p.err)) {
-          ok = false;
-          break;
-        }
-        mx = fmaxf(mx, bars->xmax[gs & 1][half ^ 1][r]) * p.qscale;
+        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(s[c]));
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                         p.qscale;
         float alpha = 1.f;
         bool rescale = false;
         if (mx > m + 8.f) {
@@ -392,104 +410,77 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         float rs8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) rs8[e] = 0.f;
+        for (int x = 0; x < 8; ++x) rs8[x] = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
+        for (int cc = 0; cc < 4; ++cc) {
           uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2(fmaf(__uint_as_float(s[cc * 32 + 2 * e]), p.qscale, -m));
-            const float p1 = ex2(fmaf(__uint_as_float(s[cc * 32 + 2 * e + 1]), p.qscale, -m));
-            rs8[e & 7] += p0 + p1;
-            pk[e] = pack_bf16x2(p0, p1);
+          for (int x = 0; x < 16; ++x) {
+            const float p0 = ex2(fmaf(__uint_as_float(s[cc * 32 + 2 * x]), p.qscale, -m));
+            const float p1 = ex2(fmaf(__uint_as_float(s[cc * 32 + 2 * x + 1]), p.qscale, -m));
+            rs8[x & 7] += p0 + p1;
+            pk[x] = pack_bf16x2(p0, p1);
           }
-          // P overwrites the S columns this warp has already read
-          tmem_st16(s_tm + half * 64 + cc * 16, pk);
+          tmem_st16(s_tm + cc * 16, pk);  // P over the S columns already read
         }
-        const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+        const float rs =
+            ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         l = fmaf(l, alpha, rs);
         // tcgen05.ld / st are warp-collective: the whole warp rescales its O rows
         // when any of its rows raised the max (the others multiply by alpha = 1).
+        // Every PV of this tile issued so far has completed (see above).
         if (__any_sync(0xffffffffu, rescale)) {
-          if (!warp_wait(&bars->o_done, (gs - 1) & 1, p.err)) {  // PV of the previous tile done
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
-            const uint32_t oc = tmem + lane_off + C::O_COL + ob * 128 + half * (D / 2) + c * 32;
-            tmem_ld32(oc, o);
+            tmem_ld32(o_tm + c * 32, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(oc, o);
+            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+            tmem_st32(o_tm + c * 32, o);
           }
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars->p_ready[sb]);
+        mbar_arrive(&bars->p_ready[t]);
       }
       if (!ok) break;
-      // Hand the row statistics to the epilogue. The slots of this O buffer
-      // were last read by the epilogue of item j - 2.
-      if (j >= 2 && !warp_wait(&bars->o_free[ob], ((j >> 1) - 1) & 1, p.err)) break;
-      bars->lsum[ob][half][r] = l;
-      if (half == 0) bars->lmax[ob][r] = m;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->l_ready[ob]);
-      g += nkt;
-    }
-  } else {
-    // ---------------------------------------------------------------- epilogue
-    // One warp per lane quadrant: reads the item's O rows out of TMEM in
-    // 32-column chunks, normalises them and writes them with TMA stores
-    // through a 4 KB staging tile (128-byte swizzle: chunk q of row i at
-    // ((q ^ (i & 7)) * 16), which keeps the shared-memory writes conflict free).
-    const int quad = warp & 3;
-    const int r = quad * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    uint8_t* stg = sStage + (warp - kWarpEpi0) * C::STAGE_BYTES;
-    int j = 0;
-    for (int it = blockIdx.x; it < p.items; it += gridDim.x, ++j) {
-      int row, rank;
-      item_coords(it, p.rows, p.nqt, p.rb, row, rank);
-      const int qt = p.nqt - 1 - rank;
-      const int ob = j & 1;
-      const int qrow = qt * BM + r;
-      const int tok0 = qt * BM + quad * 32;  // first token of this warp's rows
-      if (!warp_wait(&bars->o_last[ob], (j >> 1) & 1, p.err) ||
-          !warp_wait(&bars->l_ready[ob], (j >> 1) & 1, p.err))
-        break;
+      // ---- epilogue: O out of TMEM (then the next item's PVs may use it),
+      // normalised and written with TMA stores through two 2 KB staging tiles
+      // per warp (64-byte swizzle: chunk q of row i at ((q ^ ((i >> 1) & 3)) * 16),
+      // which keeps the shared-memory writes conflict free).
+      if (!warp_wait(&bars->o_last[t], e & 1, p.err)) break;
       tc_fence_after();
-      const float lrow = bars->lsum[ob][0][r] + bars->lsum[ob][1][r];
-      const float inv = 1.f / lrow;
-      if (qrow < p.T) p.lse2[static_cast<size_t>(row) * p.Tp + qrow] = bars->lmax[ob][r] + log2f(lrow);
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_off + C::O_COL + ob * 128 + c * 32, o);
-        tmem_wait_ld();
-        if (c == D / 32 - 1) {  // O buffer fully read: the item after next may use it
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->o_free[ob]);
-        }
-        if (lane == 0) bulk_wait_read_all();  // the previous store has read the staging tile
+      uint32_t o[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(o_tm + c * 32, o + c * 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->o_free[t]);
+      const float inv = 1.f / l;
+      if (qrow < p.T) p.lse2[static_cast<size_t>(row) * p.Tp + qrow] = m + log2f(l);
+      const int tok0 = qt * BM + quad * 32;  // first token of this warp's rows
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c, ++rounds) {
+        uint8_t* stg = sStage + (sw * 2 + (rounds & 1)) * C::STAGE_BYTES;
+        if (lane == 0) bulk_wait_read_1();  // the store that last used this tile has read it
         __syncwarp();
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<float4*>(stg + lane * 128 + ((q ^ (lane & 7)) << 4)) =
-              make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
-                          __uint_as_float(o[4 * q + 2]) * inv, __uint_as_float(o[4 * q + 3]) * inv);
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<float4*>(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) = make_float4(
+              __uint_as_float(o[16 * c + 4 * q]) * inv, __uint_as_float(o[16 * c + 4 * q + 1]) * inv,
+              __uint_as_float(o[16 * c + 4 * q + 2]) * inv,
+              __uint_as_float(o[16 * c + 4 * q + 3]) * inv);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && tok0 < p.T) {  // rows past the prompt end are clipped by the map
-          tma_store_3d(&to, stg, c * 32, tok0, row);
+        if (lane == 0) {
+          if (tok0 < p.T) tma_store_3d(&to, stg, c * 16, tok0, row);  // rows past T are clipped
           bulk_commit();
         }
       }
+      n += qt + 1;
+      ++e;
     }
     if (lane == 0) bulk_wait_all();
   }
@@ -837,7 +828,7 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int rows, int T, int D) {
 }
 
 // Output [rows, T, D] fp32 as the target of the epilogue's TMA stores: boxes
-// of 32 tokens x 32 channels (128 bytes, 128-byte swizzle); tokens past T are
+// of 32 tokens x 16 channels (64 bytes, 64-byte swizzle); tokens past T are
 // clipped, so the last tile of a row never writes into the next row.
 cudaError_t make_store_map(CUtensorMap* m, void* base, int rows, int T, int D) {
   auto enc = tensor_map_encoder();
@@ -845,10 +836,10 @@ cudaError_t make_store_map(CUtensorMap* m, void* base, int rows, int T, int D) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T),
                         static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(T) * D * 4};
-  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t box[3] = {16, 32, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -869,8 +860,8 @@ cudaError_t forward_t(const void* Q, const void* K, const void* V, int rows, int
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int nqt = (T + BM - 1) / BM;
-  FwdParams p{lse2, rows, T, lse_stride(T), nqt, rows * nqt, rows_per_l2_block(T, D, 2),
+  const int nqt = (T + BM - 1) / BM, nqb = (nqt + 1) / 2;
+  FwdParams p{lse2, rows, T, lse_stride(T), nqt, nqb, rows * nqb, rows_per_l2_block(T, D, 2),
               kLog2e / sqrtf(float(D)), err};
   const unsigned grid = static_cast<unsigned>(std::min(p.items, num_sms()));
   attn_fwd_kernel<D><<<grid, kFwdThreads, FwdCfg<D>::SMEM, stream>>>(mq, mk, mv, mo, p);

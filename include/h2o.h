@@ -26,6 +26,8 @@
  *     h2o_last_evicted and h2o_sync_check synchronise with the host.
  *   - The library owns the cache. It allocates it from PyTorch's CUDA caching
  *     allocator and frees it in h2o_destroy. PyTorch serves for nothing else.
+ *   - Prompt tensors Q, K, V and prefill outputs `out` are moved by TMA and
+ *     must be 16-byte aligned (any CUDA allocation is); otherwise H2O_EINVAL.
  *   - Layouts: Q, K, V of a prompt are bf16, contiguous [batch, heads, T, d];
  *     decode inputs q, k_new, v_new are bf16, contiguous [batch, heads, d];
  *     outputs are fp32 in the same layouts. head_dim d is 64 or 128. Logits

@@ -54,3 +54,17 @@ def test_null_context_calls_fail_cleanly_without_gpu(lib):
     out = ctypes.c_void_p()
     assert lib.h2o_create(1, 1, 1, 96, 1, 1, ctypes.byref(out)) == -1
     assert out.value is None
+
+
+def test_misaligned_prompt_buffers_are_rejected_without_gpu(lib):
+    """TMA needs 16-byte aligned prompt tensors and outputs; the check runs
+    before any CUDA call (the addresses are never dereferenced)."""
+    lib.h2o_last_error.restype = ctypes.c_char_p
+    for fn, n_tail in ((lib.h2o_prefill_attention, 2), (lib.h2o_prefill_attention_noalloc, 3)):
+        fn.restype = ctypes.c_int
+        fn.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p] * n_tail
+    good, bad = 0x10000, 0x10004
+    assert lib.h2o_prefill_attention(good, good, good, 2, 256, 128, bad, good) == -1
+    assert b"16-byte aligned" in lib.h2o_last_error()
+    assert lib.h2o_prefill_attention_noalloc(bad, good, good, 2, 256, 128, good, good, None) == -1
+    assert b"16-byte aligned" in lib.h2o_last_error()
