@@ -22,7 +22,8 @@
 // (fill count, next position) and the arrival counters live in device memory
 // and are advanced / reset here, so a CUDA graph of many steps replays
 // correctly. The launch uses programmatic dependent launch: the next step's
-// CTAs run their prologue while this step drains.
+// CTAs are scheduled while this step drains and read nothing before their
+// dependency wait.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -101,7 +102,10 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   const int cap = max(0, min(a.seg_len, a.k - s0));
   const size_t rk = static_cast<size_t>(row) * a.k;
 
-  // ---- prologue: this step's inputs do not depend on the previous step.
+  // Everything before this wait overlaps the previous kernel's tail.
+  grid_dependency_wait();  // the cache, scores and metadata are written by the previous step
+  // ---- inputs. They are read after the dependency wait: the kernel before
+  // this one in the stream may have written q, k_new or v_new.
   float qf[8];
   {
     const uint4 qv = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
@@ -120,7 +124,6 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) sm.vnew[l * 8 + i] = vf[i];
   }
-  grid_dependency_wait();  // the cache, scores and metadata are written by the previous step
 
   const int32_t* meta = a.meta + static_cast<size_t>(row) * 4;
   const int count = meta[0];

@@ -266,24 +266,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       uint32_t g = 0, n0 = 0, n1 = 0, e1 = 0;
       bool ok = true;
       int j = 0;
+      // Descriptors of the operand tiles are computed once; a stage or k-step
+      // only adds its byte offset (>> 4) to the start-address field, so each
+      // MMA costs one 64-bit add and the instruction.
+      const uint64_t dq0 = desc_kmajor<D>(sQ, 0), dk0 = desc_kmajor<D>(sK, 0);
+      const uint64_t dv0 = smem_desc(sV, kBoxBytes, 1024);
       auto pv = [&](int t, uint32_t gp, bool first) {
-        const uint8_t* v_tile = sV + (gp % C::VST) * C::TILE;
+        // B = V tile, MN-major: 16 keys = two 8-row swizzle atoms (2048 B);
+        // the two 64-column halves of d sit one TMA box (16 KB) apart.
+        const uint64_t vb = dv0 + static_cast<uint64_t>((gp % C::VST) * (C::TILE >> 4));
+        const uint32_t d_tm = tmem + C::O_COL + t * 128, a_tm = tmem + t * 128;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // B = V tile, MN-major: 16 keys = two 8-row swizzle atoms (2048 B);
-          // the two 64-column halves of d sit one TMA box (16 KB) apart.
-          const uint64_t bdesc = smem_desc(v_tile + kk * 2048, kBoxBytes, 1024);
-          umma_ts(tmem + C::O_COL + t * 128, tmem + t * 128 + kk * 8, bdesc, idesc_pv,
-                  (!first || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_ts(d_tm, a_tm + kk * 8, vb + kk * (2048 >> 4), idesc_pv, (!first || kk > 0) ? 1u : 0u);
       };
       auto qk = [&](int t, uint32_t gk) {
-        const uint8_t* k_tile = sK + (gk % C::KST) * C::TILE;
-        const uint8_t* q_tile = sQ + t * C::TILE;
+        const uint64_t kb = dk0 + static_cast<uint64_t>((gk % C::KST) * (C::TILE >> 4));
+        const uint64_t qb = dq0 + static_cast<uint64_t>(t * (C::TILE >> 4));
+        const uint32_t d_tm = tmem + t * 128;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + t * 128, desc_kmajor<D>(q_tile, kk), desc_kmajor<D>(k_tile, kk),
-                  idesc_qk, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+          umma_ss(d_tm, qb + off, kb + off, idesc_qk, kk > 0);
+        }
       };
       for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x, ++j) {
         int row, rank;
@@ -629,6 +634,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
     // S^T = K Q^T with K from TMEM (A) and the query tile from shared memory (B).
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(BN, BM, 0, 0);  // M = keys, N = queries
+      const uint64_t dq0 = desc_kmajor<D>(sQ, 0);  // query stage s adds s * TILE >> 4
       uint32_t g = 0;
       for (int j = 0; j < n_items; ++j) {
         int row, kt;
@@ -646,11 +652,12 @@ __global__ void __launch_bounds__(kColThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint8_t* q_tile = sQ + st * C::TILE;
+          const uint64_t qd = dq0 + static_cast<uint64_t>(st * (C::TILE >> 4));
+          const uint32_t d_tm = tmem + sb * 128, a_tm = tmem + C::KA_COL + kb * (D / 2);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            umma_ts(tmem + sb * 128, tmem + C::KA_COL + kb * (D / 2) + kk * 8,
-                    desc_kmajor<D>(q_tile, kk), idesc, kk > 0);
+            umma_ts(d_tm, a_tm + kk * 8, qd + (((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4), idesc,
+                    kk > 0);
           umma_commit(&bars->s_full[sb]);
           umma_commit(&bars->q_empty[st]);
         }
