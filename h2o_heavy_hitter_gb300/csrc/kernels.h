@@ -62,10 +62,11 @@ cudaError_t decode_launch(const DecodeArgs& a, const DecodeConfig& cfg, int rows
 inline int lse_stride(int T) { return (T + 127) / 128 * 128; }
 
 // Causal attention over `rows` rows of T tokens: O (fp32 [rows][T][d]) and the
-// base-2 log-sum-exp of each query row's scaled logits (fp32 [rows][lse_stride(T)]).
+// negated base-2 log-sum-exp of each query row's scaled logits, -lse2
+// (fp32 [rows][lse_stride(T)]).
 cudaError_t prefill_forward(const void* Q, const void* K, const void* V, int rows, int T, int d,
                             float* O, float* lse2, int32_t* err, cudaStream_t stream);
-// Column sums of the causal probability matrix (fp32 [rows][T]), given lse2.
+// Column sums of the causal probability matrix (fp32 [rows][T]), given -lse2.
 cudaError_t prefill_colsum(const void* Q, const void* K, const float* lse2, int rows, int T,
                            int d, float* colsum, int32_t* err, cudaStream_t stream);
 // Device address of the library's fixed log-sum-exp array used by

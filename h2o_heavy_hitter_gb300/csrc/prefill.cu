@@ -400,11 +400,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         float mx8[8];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) mx8[x] = __uint_as_float(s[x]);
+        for (int x = 0; x < 8; ++x) mx8[x] = fmaxf(__uint_as_float(s[x]), __uint_as_float(s[x + 8]));
 #pragma unroll
-        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(s[c]));
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+        for (int c = 16; c < 128; c += 16)
+#pragma unroll
+          for (int x = 0; x < 8; ++x)
+            mx8[x] = fmax3(mx8[x], __uint_as_float(s[c + x]), __uint_as_float(s[c + 8 + x]));
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7])) *
                          p.qscale;
         float alpha = 1.f;
         bool rescale = false;
@@ -413,23 +416,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           rescale = kt > 0;
           m = mx;
         }
-        float rs8[8];
+        // p = 2^(s * qscale - m), two keys per packed fma / add
+        const uint64_t sc2 = f2_pack(p.qscale, p.qscale), nm2 = f2_pack(-m, -m);
+        uint64_t rs2[4];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) rs8[x] = 0.f;
+        for (int x = 0; x < 4; ++x) rs2[x] = f2_pack(0.f, 0.f);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t pk[16];
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t pk[8];
 #pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const float p0 = ex2(fmaf(__uint_as_float(s[cc * 32 + 2 * x]), p.qscale, -m));
-            const float p1 = ex2(fmaf(__uint_as_float(s[cc * 32 + 2 * x + 1]), p.qscale, -m));
-            rs8[x & 7] += p0 + p1;
+          for (int x = 0; x < 8; ++x) {
+            float a, b;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[cc * 16 + 2 * x]),
+                                     __uint_as_float(s[cc * 16 + 2 * x + 1])),
+                             sc2, nm2),
+                      a, b);
+            const float p0 = ex2(a), p1 = ex2(b);
+            rs2[x & 3] = f2_add(rs2[x & 3], f2_pack(p0, p1));
             pk[x] = pack_bf16x2(p0, p1);
           }
-          tmem_st16(s_tm + cc * 16, pk);  // P over the S columns already read
+          tmem_st8(s_tm + cc * 8, pk);  // P over the S columns already read
         }
+        float rsv[8];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) f2_unpack(rs2[x], rsv[2 * x], rsv[2 * x + 1]);
         const float rs =
-            ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+            ((rsv[0] + rsv[1]) + (rsv[2] + rsv[3])) + ((rsv[4] + rsv[5]) + (rsv[6] + rsv[7]));
         l = fmaf(l, alpha, rs);
         // tcgen05.ld / st are warp-collective: the whole warp rescales its O rows
         // when any of its rows raised the max (the others multiply by alpha = 1).
@@ -464,7 +476,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->o_free[t]);
       const float inv = 1.f / l;
-      if (qrow < p.T) p.lse2[static_cast<size_t>(row) * p.Tp + qrow] = m + log2f(l);
+      if (qrow < p.T) p.lse2[static_cast<size_t>(row) * p.Tp + qrow] = -(m + log2f(l));
       const int tok0 = qt * BM + quad * 32;  // first token of this warp's rows
 #pragma unroll
       for (int c = 0; c < D / 16; ++c, ++rounds) {
@@ -734,35 +746,49 @@ __global__ void __launch_bounds__(kColThreads, 1)
         }
         const float* L = sL + ls * BM + cb;
         const int qvalid = min(BM, p.T - qt * BM) - cb;  // queries past the prompt end are padding
-        // Eight independent sums; the LSE values come as float4 loads.
-        float a8[8];
+        // L holds -lse2 of each query: p = 2^(s * qscale - lse2), two queries per
+        // packed fma / add; the LSE values come as float4 loads.
+        const uint64_t sc2 = f2_pack(p.qscale, p.qscale);
+        uint64_t a2[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) a8[e] = 0.f;
+        for (int e = 0; e < 4; ++e) a2[e] = f2_pack(0.f, 0.f);
         if (i == 0 || qvalid < 64) {
           const int c0 = i == 0 ? r - cb : 0;  // diagonal tile: queries >= key r only
 #pragma unroll
           for (int c4 = 0; c4 < 64; c4 += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(L + c4);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            float x[4];
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c4]), __uint_as_float(s[c4 + 1])), sc2,
+                             f2_pack(l4.x, l4.y)),
+                      x[0], x[1]);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c4 + 2]), __uint_as_float(s[c4 + 3])), sc2,
+                             f2_pack(l4.z, l4.w)),
+                      x[2], x[3]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int c = c4 + e;
-              const float x = ex2(fmaf(__uint_as_float(s[c]), p.qscale, -lv[e]));
-              a8[c & 7] += (c >= c0 && c < qvalid) ? x : 0.f;
+              x[e] = (c >= c0 && c < qvalid) ? ex2(x[e]) : 0.f;
             }
+            a2[(c4 >> 2) & 3] = f2_add(a2[(c4 >> 2) & 3], f2_add(f2_pack(x[0], x[1]), f2_pack(x[2], x[3])));
           }
         } else {
 #pragma unroll
           for (int c4 = 0; c4 < 64; c4 += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(L + c4);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = c4 + e;
-              a8[c & 7] += ex2(fmaf(__uint_as_float(s[c]), p.qscale, -lv[e]));
-            }
+            float x0, x1, x2, x3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c4]), __uint_as_float(s[c4 + 1])), sc2,
+                             f2_pack(l4.x, l4.y)),
+                      x0, x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c4 + 2]), __uint_as_float(s[c4 + 3])), sc2,
+                             f2_pack(l4.z, l4.w)),
+                      x2, x3);
+            a2[(c4 >> 2) & 3] = f2_add(a2[(c4 >> 2) & 3],
+                                       f2_add(f2_pack(ex2(x0), ex2(x1)), f2_pack(ex2(x2), ex2(x3))));
           }
         }
+        float a8[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f2_unpack(a2[e], a8[2 * e], a8[2 * e + 1]);
         acc += ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->l_empty[ls]);
