@@ -53,6 +53,8 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
+from . import kv_fp8
+
 NEAR_TIE = 1e-4  # relative margin below which an eviction decision is a near-tie
 
 
@@ -144,6 +146,13 @@ class RowCache:
     V: np.ndarray  # float64 [n, d]
     score: np.ndarray  # float64 [n]
     t: int  # position of the next token to be decoded
+    # With an FP8 cache (kv_fp8 module): K and V hold the dequantised tokens and
+    # these arrays the stored codes [n, d] (uint8) and scales [n] (float32).
+    kv_fp8: bool = False
+    Kc: np.ndarray | None = None
+    Ks: np.ndarray | None = None
+    Vc: np.ndarray | None = None
+    Vs: np.ndarray | None = None
 
     @property
     def k(self) -> int:
@@ -160,12 +169,25 @@ class PrefillResult:
     margin: float
 
 
+def _quantized(X: np.ndarray):
+    """Codes, scales and dequantised rows of token vectors X [n, d] (kv_fp8)."""
+    n, d = X.shape
+    codes = np.zeros((n, d), dtype=np.uint8)
+    scales = np.zeros(n, dtype=np.float32)
+    for i in range(n):
+        codes[i], scales[i] = kv_fp8.quantize_vector(X[i])
+    deq = np.array([kv_fp8.dequantize_vector(codes[i], scales[i]) for i in range(n)]).reshape(n, d)
+    return codes, scales, deq
+
+
 def prefill(Q, K, V, h: int, r: int, scale: float | None = None,
-            row_block: int | None = None) -> PrefillResult:
+            row_block: int | None = None, kv_fp8_cache: bool = False) -> PrefillResult:
     """Prefill one row: causal attention, column-sum scores, selection.
 
     Retained tokens carry their prefill column sums forward as their
-    accumulated scores."""
+    accumulated scores. With ``kv_fp8_cache`` the attention still runs on the
+    full-precision prompt and the retained tokens are stored quantised
+    (kv_fp8 module)."""
     K = np.asarray(K, dtype=np.float64)
     V = np.asarray(V, dtype=np.float64)
     d = K.shape[1]
@@ -175,6 +197,10 @@ def prefill(Q, K, V, h: int, r: int, scale: float | None = None,
     kept, margin = prefill_select(colsum, h, r)
     cache = RowCache(h, r, scale, kept.copy(), K[kept].copy(), V[kept].copy(),
                      colsum[kept].copy(), K.shape[0])
+    if kv_fp8_cache:
+        cache.kv_fp8 = True
+        cache.Kc, cache.Ks, cache.K = _quantized(cache.K)
+        cache.Vc, cache.Vs, cache.V = _quantized(cache.V)
     return PrefillResult(cache, O, colsum, lse, kept, margin)
 
 
@@ -207,9 +233,17 @@ def decode_step(c: RowCache, q, k_new, v_new) -> StepLog:
       5. the survivors form the new retained set."""
     q = np.asarray(q, dtype=np.float64)
     t = c.t
+    k_new = np.asarray(k_new, dtype=np.float64)
+    v_new = np.asarray(v_new, dtype=np.float64)
+    if c.kv_fp8:  # the new token is stored quantised before it is attended to
+        kc, ks, k_new = _quantized(k_new[None, :])
+        vc, vs, v_new = _quantized(v_new[None, :])
+        Kc, Ks = np.vstack([c.Kc, kc]), np.append(c.Ks, ks)
+        Vc, Vs = np.vstack([c.Vc, vc]), np.append(c.Vs, vs)
+        k_new, v_new = k_new[0], v_new[0]
     pos = np.append(c.pos, t)
-    K = np.vstack([c.K, np.asarray(k_new, dtype=np.float64)[None, :]])
-    V = np.vstack([c.V, np.asarray(v_new, dtype=np.float64)[None, :]])
+    K = np.vstack([c.K, k_new[None, :]])
+    V = np.vstack([c.V, v_new[None, :]])
     s = c.scale * (K @ q)
     e = np.exp(s - s.max())
     p = e / e.sum()
@@ -231,8 +265,12 @@ def decode_step(c: RowCache, q, k_new, v_new) -> StepLog:
         keep = np.ones(pos.shape[0], dtype=bool)
         keep[e_idx] = False
         pos, K, V, score = pos[keep], K[keep], V[keep], score[keep]
+        if c.kv_fp8:
+            Kc, Ks, Vc, Vs = Kc[keep], Ks[keep], Vc[keep], Vs[keep]
 
     c.pos, c.K, c.V, c.score, c.t = pos, K, V, score, t + 1
+    if c.kv_fp8:
+        c.Kc, c.Ks, c.Vc, c.Vs = Kc, Ks, Vc, Vs
     return StepLog(out, p, pos_attended, evicted, margin, n_cand, ev_score)
 
 
@@ -251,12 +289,12 @@ class RowTrace:
 
 def run_row(q_all, k_all, v_all, T: int, S: int, h: int, r: int,
             scale: float | None = None, row_block: int | None = None,
-            keep_sets: bool = True) -> RowTrace:
+            keep_sets: bool = True, kv_fp8_cache: bool = False) -> RowTrace:
     """Prefill tokens [0, T) then decode tokens T .. T+S-1 of one row."""
     q_all = np.asarray(q_all, dtype=np.float64)
     k_all = np.asarray(k_all, dtype=np.float64)
     v_all = np.asarray(v_all, dtype=np.float64)
-    pre = prefill(q_all[:T], k_all[:T], v_all[:T], h, r, scale, row_block)
+    pre = prefill(q_all[:T], k_all[:T], v_all[:T], h, r, scale, row_block, kv_fp8_cache)
     tr = RowTrace(pre)
     c = pre.cache
     for s in range(S):

@@ -49,6 +49,7 @@ def _load_mutant(name, old, new):
     modname = "oracle_mutant_" + "".join(ch if ch.isalnum() else "_" for ch in name)
     mod = types.ModuleType(modname)
     mod.__file__ = SRC
+    mod.__package__ = "oracle"  # the oracle's relative imports resolve in its package
     sys.modules[modname] = mod
     try:
         exec(compile(src, SRC, "exec"), mod.__dict__)
