@@ -239,9 +239,11 @@ L2_FALLBACK_BYTES = 129 << 20
 MAX_CYCLED_LAYERS = 64     # tiny caches stay latency-bound; they are not cycled
 
 
-def _layer_cache_bytes(w):
-    """Device bytes of one layer's cache: K, V (bf16), score (fp32), position (int32)."""
-    return w.rows_per_layer * w.k * (4 * w.head_dim + 8)
+def _layer_cache_bytes(w, kv="bf16"):
+    """Device bytes of one layer's cache: K, V (bf16, or E4M3 codes plus two fp32
+    scales), score (fp32), position (int32)."""
+    per_slot = 4 * w.head_dim + 8 if kv == "bf16" else 2 * w.head_dim + 16
+    return w.rows_per_layer * w.k * per_slot
 
 
 def _default_steps(w):
@@ -335,7 +337,7 @@ def run_ours(args, w):
     h_pre_out = torch.empty(pre_out.shape, dtype=torch.float32).pin_memory()
     h_dec_out = torch.empty(dec_out.shape, dtype=torch.float32).pin_memory()
 
-    ctx = h2o.h2o_create(L, B, H, d, w.h, w.r)
+    ctx = h2o.h2o_create(L, B, H, d, w.h, w.r, kv=args.kv)
     stream = torch.cuda.Stream(device=dev)
 
     def prefill_all(c, layers):
@@ -428,10 +430,10 @@ def run_ours(args, w):
     # twice the L2 size in all) makes every launch read its cache from HBM, as
     # the layers of a deep model would, with launches still back to back.
     cycled_ms, n_cycle = None, 0
-    need = -(-2 * l2_bytes // _layer_cache_bytes(w))
-    if _layer_cache_bytes(w) * L <= l2_bytes and need <= MAX_CYCLED_LAYERS:
+    need = -(-2 * l2_bytes // _layer_cache_bytes(w, args.kv))
+    if _layer_cache_bytes(w, args.kv) * L <= l2_bytes and need <= MAX_CYCLED_LAYERS:
         n_cycle = max(2, need)
-        ctx_c = h2o.h2o_create(n_cycle, B, H, d, w.h, w.r)
+        ctx_c = h2o.h2o_create(n_cycle, B, H, d, w.h, w.r, kv=args.kv)
         sc = min(S, 32)
         with torch.cuda.stream(stream):
             prefill_all(ctx_c, n_cycle)
@@ -479,7 +481,7 @@ def run_ours(args, w):
 
     peaks, peak_kind = _peaks()
     rows = B * H
-    bytes_per_launch = decode_bytes_per_row_step(w.k, d) * rows
+    bytes_per_launch = decode_bytes_per_row_step(w.k, d, args.kv) * rows
     dec_launch_ms = decode_ms / (S * L)  # graph replay: launch gaps included
     achieved = bytes_per_launch / (dec_launch_ms * 1e-3) / 1e9
     achieved_cold = bytes_per_launch / (cold_ms * 1e-3) / 1e9
@@ -490,7 +492,7 @@ def run_ours(args, w):
     value = tokens / (elapsed_ms * 1e-3)
     roof = {"kernel": "h2o decode_kernel", "bound": "hbm", "achieved": achieved,
             "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-            "traffic": _profiled_traffic("decode.cu", w.name),
+            "traffic": _profiled_traffic("decode.cu", w.name) if args.kv == "bf16" else None,
             "bytes_per_launch": bytes_per_launch,
             "launch_ms": dec_launch_ms,
             "peak_source": f"{peak_kind} hbm_gbs"}
@@ -504,7 +506,7 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": _data_desc(w),
-        "config": _config(w, l2_bytes),
+        "config": dict(_config(w, l2_bytes), kv_cache=args.kv),
         "roofline": roof,
         "phases": {"prefill_ms": prefill_ms, "decode_ms": decode_ms,
                    "prefill_tokens_per_s": B * T * L / (prefill_ms * 1e-3),
@@ -536,6 +538,8 @@ def main():
     ap.add_argument("--workload", default="opt-6.7b-layer", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
+                    help="cache storage: bf16, or E4M3 codes with per-token scales")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

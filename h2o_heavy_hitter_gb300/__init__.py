@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "H2OError", "H2OContext", "load_library", "h2o_create", "h2o_destroy", "h2o_prefill",
     "h2o_decode_step", "h2o_prefill_attention", "h2o_cache_positions", "h2o_last_evicted",
-    "h2o_cache_view", "h2o_sync_check", "LIB_PATH",
+    "h2o_cache_view", "h2o_cache_scales", "h2o_sync_check", "LIB_PATH", "KV_FORMATS",
 ]
 
 LIB_PATH = Path(__file__).resolve().parent / "libh2o.so"
@@ -29,6 +29,8 @@ H2O_OK, H2O_EINVAL, H2O_ESTATE, H2O_ENOMEM, H2O_ECUDA, H2O_EDEVICE = 0, -1, -2, 
 _ERR_NAMES = {-1: "EINVAL", -2: "ESTATE", -3: "ENOMEM", -4: "ECUDA", -5: "EDEVICE"}
 
 _lib = None
+
+KV_FORMATS = {"bf16": 0, "fp8": 1}  # H2O_KV_BF16, H2O_KV_FP8
 
 
 class H2OError(RuntimeError):
@@ -49,6 +51,8 @@ def load_library() -> ctypes.CDLL:
     I32P = ctypes.POINTER(ctypes.c_int32)
     sig = {
         "h2o_create": (I, [I, I, I, I, I, I, ctypes.POINTER(P)]),
+        "h2o_create_ex": (I, [I, I, I, I, I, I, I, ctypes.POINTER(P)]),
+        "h2o_cache_scales": (I, [P, I, ctypes.POINTER(P), ctypes.POINTER(P)]),
         "h2o_destroy": (None, [P]),
         "h2o_prefill": (I, [P, I, P, P, P, I, P]),
         "h2o_decode_step": (I, [P, I, P, P, P, P]),
@@ -100,8 +104,9 @@ class H2OContext:
     """Owner of one h2o_ctx handle (cache of `layers` layers)."""
 
     def __init__(self, handle: int, layers: int, batch: int, heads: int, head_dim: int, h: int,
-                 r: int):
+                 r: int, kv: str = "bf16"):
         self.handle = handle
+        self.kv = kv
         self.layers, self.batch, self.heads, self.head_dim = layers, batch, heads, head_dim
         self.h, self.r, self.k = h, r, h + r
         self.rows = batch * heads
@@ -124,12 +129,21 @@ class H2OContext:
         self.close()
 
 
-def h2o_create(layers: int, batch: int, heads: int, head_dim: int, h: int, r: int) -> H2OContext:
+def h2o_create(layers: int, batch: int, heads: int, head_dim: int, h: int, r: int,
+               kv: str = "bf16") -> H2OContext:
+    """Cache of `layers` layers; kv "bf16" (h2o_create) or "fp8" (E4M3 codes with
+    per-token scales, h2o_create_ex)."""
     _need_cuda()
+    if kv not in KV_FORMATS:
+        raise ValueError(f"kv must be one of {sorted(KV_FORMATS)}")
     lib = load_library()
     out = ctypes.c_void_p()
-    _check(lib.h2o_create(layers, batch, heads, head_dim, h, r, ctypes.byref(out)))
-    return H2OContext(out.value, layers, batch, heads, head_dim, h, r)
+    if kv == "bf16":
+        _check(lib.h2o_create(layers, batch, heads, head_dim, h, r, ctypes.byref(out)))
+    else:
+        _check(lib.h2o_create_ex(layers, batch, heads, head_dim, h, r, KV_FORMATS[kv],
+                                 ctypes.byref(out)))
+    return H2OContext(out.value, layers, batch, heads, head_dim, h, r, kv)
 
 
 def h2o_destroy(ctx: H2OContext) -> None:
@@ -204,21 +218,37 @@ class _DeviceArray:
 def h2o_cache_view(ctx: H2OContext, layer: int) -> dict:
     """Zero-copy torch views of one layer's cache arrays (library-owned memory).
 
-    K and V are returned as int16 views of the bf16 bits (view(torch.bfloat16)
-    to reinterpret)."""
+    K and V are bf16 tensors, or uint8 E4M3 codes for an "fp8" cache (its
+    scales: h2o_cache_scales)."""
     ptrs = [ctypes.c_void_p() for _ in range(5)]
     _check(load_library().h2o_cache_view(ctypes.c_void_p(ctx.handle), layer,
                                          *[ctypes.byref(p) for p in ptrs]))
     R, k, d = ctx.rows, ctx.k, ctx.head_dim
     dev = torch.device("cuda", torch.cuda.current_device())
     mk = lambda p, shape, ts: torch.as_tensor(_DeviceArray(p.value, shape, ts), device=dev)
+    if ctx.kv == "fp8":
+        kv_k, kv_v = mk(ptrs[0], (R, k, d), "|u1"), mk(ptrs[1], (R, k, d), "|u1")
+    else:
+        kv_k = mk(ptrs[0], (R, k, d), "<i2").view(torch.bfloat16)
+        kv_v = mk(ptrs[1], (R, k, d), "<i2").view(torch.bfloat16)
     return {
-        "K": mk(ptrs[0], (R, k, d), "<i2").view(torch.bfloat16),
-        "V": mk(ptrs[1], (R, k, d), "<i2").view(torch.bfloat16),
+        "K": kv_k,
+        "V": kv_v,
         "score": mk(ptrs[2], (R, k), "<f4"),
         "pos": mk(ptrs[3], (R, k), "<i4"),
         "meta": mk(ptrs[4], (R, 4), "<i4"),
     }
+
+
+def h2o_cache_scales(ctx: H2OContext, layer: int) -> dict:
+    """Zero-copy views of an "fp8" cache's per-slot scales: {"K": fp32 [rows, k],
+    "V": fp32 [rows, k]}."""
+    ptrs = [ctypes.c_void_p() for _ in range(2)]
+    _check(load_library().h2o_cache_scales(ctypes.c_void_p(ctx.handle), layer,
+                                           *[ctypes.byref(p) for p in ptrs]))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    mk = lambda p: torch.as_tensor(_DeviceArray(p.value, (ctx.rows, ctx.k), "<f4"), device=dev)
+    return {"K": mk(ptrs[0]), "V": mk(ptrs[1])}
 
 
 def h2o_sync_check(ctx: H2OContext) -> None:

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -122,6 +123,50 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+
+// ---- E4M3 (OCP FP8) codes ------------------------------------------------------
+// Eight codes (one per byte, element 0 in the lowest byte) to fp32; exact.
+__device__ __forceinline__ void e4m3x8_to_f32(const uint2& v, float* f) {
+  const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+          static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * h)) & 0xFFFFu), __NV_E4M3);
+      const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+      f[4 * i + 2 * h] = f2.x;
+      f[4 * i + 2 * h + 1] = f2.y;
+    }
+}
+// Two fp32 values to E4M3 codes (lo in the low byte): round to nearest even,
+// saturated to +-448.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  return __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+// Quantises the values x[0..n) of this thread, part of a token vector spread
+// over the lanes in `mask` (`lanes` of them, a power of two, adjacent): scale =
+// amax / 448 and code = E4M3(x * (448 / amax)), fp32 with one rounding per
+// operation; a zero vector gets scale 0 and zero codes. Writes the codes
+// (n / 2 pairs) and returns the scale.
+template <int N>
+__device__ __forceinline__ float quantize_e4m3(const float* x, unsigned mask, int lanes,
+                                               uint32_t* pairs) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < N; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  for (int off = lanes / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(mask, amax, off));
+  if (amax == 0.f) {
+#pragma unroll
+    for (int j = 0; j < N / 2; ++j) pairs[j] = 0u;
+    return 0.f;
+  }
+  const float inv = __fdiv_rn(448.f, amax);
+#pragma unroll
+  for (int j = 0; j < N / 2; ++j)
+    pairs[j] = f32x2_to_e4m3x2(__fmul_rn(x[2 * j], inv), __fmul_rn(x[2 * j + 1], inv));
+  return __fdiv_rn(amax, 448.f);
 }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {

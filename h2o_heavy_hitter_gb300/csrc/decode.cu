@@ -24,6 +24,8 @@
 // correctly. The launch uses programmatic dependent launch: the next step's
 // CTAs are scheduled while this step drains and read nothing before their
 // dependency wait.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -48,6 +50,39 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
                : "l"(p));
   return v;
 }
+
+__device__ __forceinline__ uint2 ldg_stream8(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+               : "=r"(v.x), "=r"(v.y)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float dot8(const uint2& kv, const float* qf) {  // E4M3 codes
+  float kf[8];
+  e4m3x8_to_f32(kv, kf);
+  float d = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) d = fmaf(qf[i], kf[i], d);
+  return d;
+}
+
+__device__ __forceinline__ void accum8(float* o, float p, const uint2& vv) {  // E4M3 codes
+  float vf[8];
+  e4m3x8_to_f32(vv, vf);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i] = fmaf(p, vf[i], o[i]);
+}
+
+// U slots' keys and values of one group batch: bf16 vectors (16 bytes per
+// lane), or E4M3 codes (8 bytes per lane) with one scale per slot.
+template <bool F8, int U>
+struct KVBatch {
+  using Vec = typename std::conditional<F8, uint2, uint4>::type;
+  Vec k[U], v[U];
+  float ks[U], vs[U];
+};
 
 __device__ __forceinline__ float dot8(const uint4& kv, const float* qf) {
   float kf[8];
@@ -88,7 +123,9 @@ struct DecodeShared {
 };
 
 // PIPE: two batches of U slots per group in flight (software pipelining).
-template <int D, int NT, int U, bool PIPE>
+// F8: the cache holds E4M3 codes with per-slot scales; the new token is
+// quantised (amax / 448 scale, fp32) before it is attended to and stored.
+template <int D, int NT, int U, bool PIPE, bool F8>
 __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   using Sm = DecodeShared<D, NT>;
   constexpr int LPS = Sm::LPS, G = Sm::G, NW = Sm::NW;
@@ -119,10 +156,12 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
     const size_t off = static_cast<size_t>(row) * D + l * 8;
     knew = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.k_new) + off);
     vnew = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.v_new) + off);
-    float vf[8];
-    bf16x8_to_f32(vnew, vf);
+    if constexpr (!F8) {
+      float vf[8];
+      bf16x8_to_f32(vnew, vf);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sm.vnew[l * 8 + i] = vf[i];
+      for (int i = 0; i < 8; ++i) sm.vnew[l * 8 + i] = vf[i];
+    }
   }
 
   const int32_t* meta = a.meta + static_cast<size_t>(row) * 4;
@@ -142,8 +181,9 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   float m = -INFINITY, lsum = 0.f, o[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) o[i] = 0.f;
-  const __nv_bfloat16* Kg = static_cast<const __nv_bfloat16*>(a.Kc) + (rk + s0) * D + l * 8;
-  const __nv_bfloat16* Vg = static_cast<const __nv_bfloat16*>(a.Vc) + (rk + s0) * D + l * 8;
+  constexpr int EB = F8 ? 1 : 2;  // bytes per cached element
+  const uint8_t* Kg = static_cast<const uint8_t*>(a.Kc) + ((rk + s0) * D + l * 8) * EB;
+  const uint8_t* Vg = static_cast<const uint8_t*>(a.Vc) + ((rk + s0) * D + l * 8) * EB;
   // A row handled by a single CTA keeps its logits in shared memory; split rows
   // hand them to the finishing CTA through the per-layer scratch.
   extern __shared__ float solo_logits[];
@@ -164,24 +204,36 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   }
   // One batch: U slots of this group, loaded by capacity (slots past the fill
   // count are masked when consumed).
-  auto load = [&](uint4 (&kv)[U], uint4 (&vv)[U], int base) {
+  using Batch = KVBatch<F8, U>;
+  auto load = [&](Batch& b, int base) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int i = base + u * G;
       if (i < cap) {
-        kv[u] = ldg_stream(Kg + static_cast<size_t>(i) * D);
-        vv[u] = ldg_stream(Vg + static_cast<size_t>(i) * D);
+        if constexpr (F8) {
+          b.k[u] = ldg_stream8(Kg + static_cast<size_t>(i) * D);
+          b.v[u] = ldg_stream8(Vg + static_cast<size_t>(i) * D);
+          b.ks[u] = __ldg(a.kscale + rk + s0 + i);
+          b.vs[u] = __ldg(a.vscale + rk + s0 + i);
+        } else {
+          b.k[u] = ldg_stream(Kg + static_cast<size_t>(i) * D * 2);
+          b.v[u] = ldg_stream(Vg + static_cast<size_t>(i) * D * 2);
+        }
       }
     }
   };
-  auto consume = [&](const uint4 (&kv)[U], const uint4 (&vv)[U], int base) {
+  auto consume = [&](const Batch& b, int base) {
     float s[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) s[u] = dot8(kv[u], qf);
+    for (int u = 0; u < U; ++u) s[u] = dot8(b.k[u], qf);
 #pragma unroll
     for (int off = LPS / 2; off > 0; off >>= 1)
 #pragma unroll
       for (int u = 0; u < U; ++u) s[u] += __shfl_xor_sync(gmask, s[u], off);
+    if constexpr (F8) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) s[u] *= b.ks[u];
+    }
     float bm = m;
 #pragma unroll
     for (int u = 0; u < U; ++u)
@@ -197,7 +249,10 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
       if (i < n) {
         const float p = ex2(s[u] - bm);
         lsum += p;
-        accum8(o, p, vv[u]);
+        if constexpr (F8)
+          accum8(o, p * b.vs[u], b.v[u]);
+        else
+          accum8(o, p, b.v[u]);
         if (l == 0) lg_out[i] = s[u];
       }
     }
@@ -206,20 +261,20 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   if constexpr (PIPE) {
     // Two batches in flight: the next batch's loads are issued before the
     // current batch is consumed, so memory is never idle between batches.
-    uint4 ka[U], va[U], kb[U], vb[U];
-    if (g < cap) load(ka, va, g);
+    Batch ba, bb;
+    if (g < cap) load(ba, g);
     for (int base = g; base < cap; base += 2 * STEP) {
-      if (base + STEP < cap) load(kb, vb, base + STEP);
-      consume(ka, va, base);
+      if (base + STEP < cap) load(bb, base + STEP);
+      consume(ba, base);
       if (base + STEP >= cap) break;
-      if (base + 2 * STEP < cap) load(ka, va, base + 2 * STEP);
-      consume(kb, vb, base + STEP);
+      if (base + 2 * STEP < cap) load(ba, base + 2 * STEP);
+      consume(bb, base + STEP);
     }
   } else {
     for (int base = g; base < cap; base += STEP) {
-      uint4 kv[U], vv[U];
-      load(kv, vv, base);
-      consume(kv, vv, base);
+      Batch b;
+      load(b, base);
+      consume(b, base);
     }
   }
   grid_launch_dependents();
@@ -252,8 +307,30 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) sm.red_o[warp][i * LPS + lane] = o[i];
   }
+  uint2 kcode = make_uint2(0, 0), vcode = make_uint2(0, 0);  // E4M3 cache: the new token
+  float kq_scale = 0.f, vq_scale = 0.f;
   if (g == 0) {  // logit of the new token (group 0 holds k_new)
-    float sn = dot8(knew, qf);
+    float sn;
+    if constexpr (F8) {
+      // quantise the new token as it will be stored; attend to the stored values
+      float kf[8], vf[8], deq[8];
+      uint32_t pr[4];
+      bf16x8_to_f32(knew, kf);
+      kq_scale = quantize_e4m3<8>(kf, gmask, LPS, pr);
+      kcode = make_uint2(pr[0] | (pr[1] << 16), pr[2] | (pr[3] << 16));
+      e4m3x8_to_f32(kcode, deq);
+      sn = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sn = fmaf(qf[i], deq[i] * kq_scale, sn);
+      bf16x8_to_f32(vnew, vf);
+      vq_scale = quantize_e4m3<8>(vf, gmask, LPS, pr);
+      vcode = make_uint2(pr[0] | (pr[1] << 16), pr[2] | (pr[3] << 16));
+      e4m3x8_to_f32(vcode, deq);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sm.vnew[l * 8 + i] = deq[i] * vq_scale;
+    } else {
+      sn = dot8(knew, qf);
+    }
 #pragma unroll
     for (int off = LPS / 2; off > 0; off >>= 1) sn += __shfl_xor_sync(gmask, sn, off);
     if (l == 0) sm.s_new = sn;
@@ -416,29 +493,55 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   const int target = sm.target;
   if (target >= 0 && g == 0) {
     const size_t dst = (rk + target) * D + l * 8;
-    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.Kc) + dst) = knew;
-    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.Vc) + dst) = vnew;
+    if constexpr (F8) {
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.Kc) + dst) = kcode;
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.Vc) + dst) = vcode;
+      if (l == 0) {
+        a.kscale[rk + target] = kq_scale;
+        a.vscale[rk + target] = vq_scale;
+      }
+    } else {
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.Kc) + dst) = knew;
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.Vc) + dst) = vnew;
+    }
   }
 }
 
 using KernelFn = void (*)(DecodeArgs);
 
-template <int D, int NT>
-KernelFn pick_u(const DecodeConfig& c) {
-  if (c.pipe) return c.unroll == 2 ? decode_kernel<D, NT, 2, true> : decode_kernel<D, NT, 4, true>;
-  return c.unroll == 2 ? decode_kernel<D, NT, 2, false> : decode_kernel<D, NT, 4, false>;
+template <int D, int NT, bool F8, bool PIPE>
+KernelFn pick_p(const DecodeConfig& c) {
+  if (c.unroll == 2) return decode_kernel<D, NT, 2, PIPE, F8>;
+  if (F8 && c.unroll == 8) return decode_kernel<D, NT, 8, PIPE, F8>;
+  return decode_kernel<D, NT, 4, PIPE, F8>;
 }
 
-KernelFn pick(const DecodeConfig& c, int d) {
-  if (d == 128) return c.threads == 256 ? pick_u<128, 256>(c) : pick_u<128, 128>(c);
-  return c.threads == 256 ? pick_u<64, 256>(c) : pick_u<64, 128>(c);
+template <int D, int NT, bool F8>
+KernelFn pick_u(const DecodeConfig& c) {
+  return c.pipe ? pick_p<D, NT, F8, true>(c) : pick_p<D, NT, F8, false>(c);
 }
+
+template <bool F8>
+KernelFn pick_f(const DecodeConfig& c, int d) {
+  if (d == 128) return c.threads == 256 ? pick_u<128, 256, F8>(c) : pick_u<128, 128, F8>(c);
+  return c.threads == 256 ? pick_u<64, 256, F8>(c) : pick_u<64, 128, F8>(c);
+}
+
+KernelFn pick(const DecodeConfig& c, int d, bool f8) { return f8 ? pick_f<true>(c, d) : pick_f<false>(c, d); }
 
 }  // namespace
 
-DecodeConfig decode_config(int rows, int k, int d, int num_sms, const DecodeTuning& tune) {
+DecodeConfig decode_config(int rows, int k, int d, int num_sms, const DecodeTuning& tune,
+                           bool fp8) {
   DecodeConfig c{};
-  c.unroll = tune.unroll == 2 || tune.unroll == 4 ? tune.unroll : 4;
+  const bool few_rows = rows < num_sms;
+  const bool many_rows = rows >= 4 * num_sms;
+  // An E4M3 slot is half the bytes of a bf16 one: with many rows (one
+  // unpipelined batch per group) twice as many slots per batch keep the same
+  // bytes in flight (measured: batch 256 x 32 heads, 194 us against 213 us).
+  c.unroll = tune.unroll == 2 || tune.unroll == 4 || (fp8 && tune.unroll == 8)
+                 ? tune.unroll
+                 : (fp8 && many_rows ? 8 : 4);
   c.pdl = tune.pdl >= 0;
   // Measured on GB300 (decode sweeps over the workload shapes):
   //  * many rows (>= 4 per SM): one 128-thread CTA per row, one batch in flight;
@@ -447,8 +550,6 @@ DecodeConfig decode_config(int rows, int k, int d, int num_sms, const DecodeTuni
   //    the serial batches of a long row;
   //  * fewer rows than SMs: rows split into segments of 128-thread CTAs until
   //    the grid covers every SM about eight times.
-  const bool few_rows = rows < num_sms;
-  const bool many_rows = rows >= 4 * num_sms;
   c.threads = tune.threads == 128 || tune.threads == 256
                   ? tune.threads
                   : (few_rows || many_rows ? 128 : 256);
@@ -483,7 +584,7 @@ cudaError_t decode_launch(const DecodeArgs& a, const DecodeConfig& cfg, int rows
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = cfg.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&lc, pick(cfg, d), a);
+  return cudaLaunchKernelEx(&lc, pick(cfg, d, a.kscale != nullptr), a);
 }
 
 }  // namespace h2o

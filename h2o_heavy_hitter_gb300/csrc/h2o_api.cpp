@@ -58,10 +58,14 @@ struct Scratch {
 struct h2o_ctx {
   int layers, batch, heads, d, h, r, k, rows;
   int device;
+  int kv_format;              // H2O_KV_BF16 or H2O_KV_FP8
   size_t kv_elems_per_layer;  // rows * k * d
+  size_t kv_elem_bytes;       // 2 (bf16) or 1 (E4M3 code)
   void* base = nullptr;       // single cache allocation
-  uint16_t* K = nullptr;
-  uint16_t* V = nullptr;
+  uint8_t* K = nullptr;
+  uint8_t* V = nullptr;
+  float* kscale = nullptr;    // E4M3 cache: per-slot key scales [layers][rows][k]
+  float* vscale = nullptr;    // E4M3 cache: per-slot value scales
   float* score = nullptr;
   int32_t* pos = nullptr;
   int32_t* meta = nullptr;
@@ -72,8 +76,10 @@ struct h2o_ctx {
   std::vector<int> prompt_len;  // per layer: -1 until prefilled
   h2o::DecodeConfig dcfg{};
 
-  void* layer_K(int l) const { return K + static_cast<size_t>(l) * kv_elems_per_layer; }
-  void* layer_V(int l) const { return V + static_cast<size_t>(l) * kv_elems_per_layer; }
+  void* layer_K(int l) const { return K + static_cast<size_t>(l) * kv_elems_per_layer * kv_elem_bytes; }
+  void* layer_V(int l) const { return V + static_cast<size_t>(l) * kv_elems_per_layer * kv_elem_bytes; }
+  float* layer_kscale(int l) const { return kscale ? kscale + static_cast<size_t>(l) * rows * k : nullptr; }
+  float* layer_vscale(int l) const { return vscale ? vscale + static_cast<size_t>(l) * rows * k : nullptr; }
   float* layer_score(int l) const { return score + static_cast<size_t>(l) * rows * k; }
   int32_t* layer_pos(int l) const { return pos + static_cast<size_t>(l) * rows * k; }
   int32_t* layer_meta(int l) const { return meta + static_cast<size_t>(l) * rows * 4; }
@@ -118,8 +124,15 @@ extern "C" {
 const char* h2o_last_error(void) { return g_error.c_str(); }
 
 int h2o_create(int layers, int batch, int heads, int head_dim, int h, int r, h2o_ctx** out) {
+  return h2o_create_ex(layers, batch, heads, head_dim, h, r, H2O_KV_BF16, out);
+}
+
+int h2o_create_ex(int layers, int batch, int heads, int head_dim, int h, int r, int kv_format,
+                  h2o_ctx** out) {
   if (!out) return fail(H2O_EINVAL, "null output pointer");
   *out = nullptr;
+  if (kv_format != H2O_KV_BF16 && kv_format != H2O_KV_FP8)
+    return fail(H2O_EINVAL, "kv_format must be H2O_KV_BF16 or H2O_KV_FP8");
   if (layers < 1 || batch < 1 || heads < 1) return fail(H2O_EINVAL, "layers, batch and heads must be >= 1");
   if (head_dim != 64 && head_dim != 128) return fail(H2O_EINVAL, "head_dim must be 64 or 128");
   if (h < 0 || r < 0 || h + r < 1 || h + r > H2O_MAX_K)
@@ -136,6 +149,8 @@ int h2o_create(int layers, int batch, int heads, int head_dim, int h, int r, h2o
   c->r = r;
   c->k = h + r;
   c->rows = static_cast<int>(rows_l);
+  c->kv_format = kv_format;
+  c->kv_elem_bytes = kv_format == H2O_KV_FP8 ? 1 : 2;
   c->prompt_len.assign(layers, -1);
   try {
     c->device = c10::cuda::current_device();
@@ -153,16 +168,18 @@ int h2o_create(int layers, int batch, int heads, int head_dim, int h, int r, h2o
   h2o::DecodeTuning tune{env_int("H2O_DECODE_THREADS"), env_int("H2O_DECODE_UNROLL"),
                          env_int("H2O_DECODE_SEGS"), env_int("H2O_DECODE_PDL"),
                          env_int("H2O_DECODE_PIPE")};
-  c->dcfg = h2o::decode_config(c->rows, c->k, c->d, sms, tune);
+  c->dcfg = h2o::decode_config(c->rows, c->k, c->d, sms, tune, kv_format == H2O_KV_FP8);
 
   const size_t L = layers, R = c->rows, K = c->k, D = head_dim;
   c->kv_elems_per_layer = R * K * D;
-  const size_t kv_bytes = align_up(L * R * K * D * 2, 256);
+  const size_t kv_bytes = align_up(L * R * K * D * c->kv_elem_bytes, 256);
   const size_t sc_bytes = align_up(L * R * K * 4, 256);
+  const size_t qs_bytes = kv_format == H2O_KV_FP8 ? sc_bytes : 0;  // per-slot scales
   const size_t meta_bytes = align_up(L * R * 16, 256);
   const size_t part_bytes = align_up(L * R * c->dcfg.segs * (D + 4) * 4, 256);
   const size_t cnt_bytes = align_up(L * R * 4, 256);
-  const size_t total = 2 * kv_bytes + 3 * sc_bytes + meta_bytes + part_bytes + cnt_bytes + 256;
+  const size_t total =
+      2 * kv_bytes + 3 * sc_bytes + 2 * qs_bytes + meta_bytes + part_bytes + cnt_bytes + 256;
   cudaStream_t s = current_stream();
   try {
     c->base = c10::cuda::CUDACachingAllocator::raw_alloc_with_stream(total, s);
@@ -171,9 +188,9 @@ int h2o_create(int layers, int batch, int heads, int head_dim, int h, int r, h2o
     return fail(H2O_ENOMEM, std::string("cache allocation failed: ") + ex.what());
   }
   char* p = static_cast<char*>(c->base);
-  c->K = reinterpret_cast<uint16_t*>(p);
+  c->K = reinterpret_cast<uint8_t*>(p);
   p += kv_bytes;
-  c->V = reinterpret_cast<uint16_t*>(p);
+  c->V = reinterpret_cast<uint8_t*>(p);
   p += kv_bytes;
   c->score = reinterpret_cast<float*>(p);
   p += sc_bytes;
@@ -187,11 +204,18 @@ int h2o_create(int layers, int batch, int heads, int head_dim, int h, int r, h2o
   p += part_bytes;
   c->counter = reinterpret_cast<int32_t*>(p);
   p += cnt_bytes;
+  if (qs_bytes) {
+    c->kscale = reinterpret_cast<float*>(p);
+    p += qs_bytes;
+    c->vscale = reinterpret_cast<float*>(p);
+    p += qs_bytes;
+  }
   c->err = reinterpret_cast<int32_t*>(p);
 
   e = cudaMemsetAsync(c->err, 0, sizeof(int32_t), s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->K, 0, 2 * kv_bytes, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->counter, 0, cnt_bytes, s);
+  if (e == cudaSuccess && qs_bytes) e = cudaMemsetAsync(c->kscale, 0, 2 * qs_bytes, s);
   for (int l = 0; l < layers && e == cudaSuccess; ++l)
     e = h2o::cache_reset(c->rows, c->k, c->layer_score(l), c->layer_pos(l), c->layer_meta(l), s);
   if (e != cudaSuccess) {
@@ -233,8 +257,12 @@ int h2o_prefill(h2o_ctx* c, int layer, const void* Q, const void* K, const void*
     e = h2o::prefill_select(static_cast<float*>(colsum.p), c->rows, T, c->h, c->r,
                             c->layer_score(layer), c->layer_pos(layer), c->layer_meta(layer), s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill select launch");
-    e = h2o::prefill_gather(K, V, c->rows, T, c->d, c->k, c->layer_pos(layer), c->layer_K(layer),
-                            c->layer_V(layer), s);
+    e = c->kv_format == H2O_KV_FP8
+            ? h2o::prefill_gather_fp8(K, V, c->rows, T, c->d, c->k, c->layer_pos(layer),
+                                      c->layer_K(layer), c->layer_V(layer),
+                                      c->layer_kscale(layer), c->layer_vscale(layer), s)
+            : h2o::prefill_gather(K, V, c->rows, T, c->d, c->k, c->layer_pos(layer),
+                                  c->layer_K(layer), c->layer_V(layer), s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill gather launch");
   } catch (const std::exception& ex) {
     return fail(H2O_ENOMEM, std::string("prefill scratch allocation failed: ") + ex.what());
@@ -288,6 +316,8 @@ int h2o_decode_step(h2o_ctx* c, int layer, const void* q, const void* k_new, con
   h2o::DecodeArgs a{};
   a.Kc = c->layer_K(layer);
   a.Vc = c->layer_V(layer);
+  a.kscale = c->layer_kscale(layer);  // null for a bf16 cache
+  a.vscale = c->layer_vscale(layer);
   a.score = c->layer_score(layer);
   a.pos = c->layer_pos(layer);
   a.meta = c->layer_meta(layer);
@@ -338,6 +368,14 @@ int h2o_cache_view(h2o_ctx* c, int layer, void** K, void** V, float** score, int
   if (score) *score = c->layer_score(layer);
   if (pos) *pos = c->layer_pos(layer);
   if (meta) *meta = c->layer_meta(layer);
+  return H2O_OK;
+}
+
+int h2o_cache_scales(h2o_ctx* c, int layer, float** k_scale, float** v_scale) {
+  if (int rc = check_layer(c, layer)) return rc;
+  if (c->kv_format != H2O_KV_FP8) return fail(H2O_EINVAL, "the cache of this context is bf16: no scales");
+  if (k_scale) *k_scale = c->layer_kscale(layer);
+  if (v_scale) *v_scale = c->layer_vscale(layer);
   return H2O_OK;
 }
 

@@ -14,8 +14,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxDecodeSegs = 64;  // most CTAs one row's decode step is split over
 
 struct DecodeArgs {
-  void* Kc;           // bf16 [rows][k][d] cached keys of one layer
-  void* Vc;           // bf16 [rows][k][d] cached values
+  void* Kc;           // [rows][k][d] cached keys of one layer: bf16, or E4M3 codes
+  void* Vc;           // [rows][k][d] cached values (same format)
+  float* kscale;      // E4M3 cache only: [rows][k] per-slot key scales (null for bf16)
+  float* vscale;      // E4M3 cache only: [rows][k] per-slot value scales
   float* score;       // [rows][k] accumulated scores
   int32_t* pos;       // [rows][k] positions (-1 empty)
   int32_t* meta;      // [rows][4] {filled, next position, last evicted, 0}
@@ -36,7 +38,7 @@ struct DecodeArgs {
 // Launch shape of the decode kernel. Zero / out-of-range values pick defaults.
 struct DecodeTuning {
   int threads;  // 128 or 256 threads per CTA
-  int unroll;   // slots per group per batch (2 or 4)
+  int unroll;   // slots per group per batch (2 or 4; 8 with an E4M3 cache)
   int segs;     // CTAs per row; 0 = automatic
   int pdl;      // < 0: launch without programmatic dependent launch
   int pipe;     // > 0: two batches per group in flight; < 0: one; 0: automatic
@@ -52,7 +54,8 @@ struct DecodeConfig {
 };
 
 // Picks the launch shape for (rows, k, d) on a device with `num_sms` SMs.
-DecodeConfig decode_config(int rows, int k, int d, int num_sms, const DecodeTuning& tune);
+DecodeConfig decode_config(int rows, int k, int d, int num_sms, const DecodeTuning& tune,
+                           bool fp8);
 cudaError_t decode_launch(const DecodeArgs& a, const DecodeConfig& cfg, int rows, int d,
                           cudaStream_t stream);
 
@@ -81,6 +84,11 @@ cudaError_t prefill_select(const float* colsum, int rows, int T, int h, int r, f
 cudaError_t prefill_gather(const void* K, const void* V, int rows, int T, int d, int k,
                            const int32_t* pos, void* Kc, void* Vc, cudaStream_t stream);
 // Resets rows to an empty cache (pos -1, score 0, meta {0, 0, -1, 0}).
+// E4M3 cache: the kept tokens quantised into their slots, codes plus one fp32
+// scale per slot for K and for V.
+cudaError_t prefill_gather_fp8(const void* K, const void* V, int rows, int T, int d, int k,
+                               const int32_t* pos, void* Kc, void* Vc, float* kscale,
+                               float* vscale, cudaStream_t stream);
 cudaError_t cache_reset(int rows, int k, float* score, int32_t* pos, int32_t* meta,
                         cudaStream_t stream);
 

@@ -169,6 +169,42 @@ __global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __rest
   }
 }
 
+// E4M3 cache: one warp per slot quantises the kept token's K and V rows
+// (D / 32 values per lane) with one scale each.
+template <int D>
+__global__ void __launch_bounds__(256) gather_fp8_kernel(const __nv_bfloat16* __restrict__ K,
+                                                        const __nv_bfloat16* __restrict__ V, int T,
+                                                        int k, const int32_t* __restrict__ pos,
+                                                        uint8_t* __restrict__ Kc,
+                                                        uint8_t* __restrict__ Vc,
+                                                        float* __restrict__ kscale,
+                                                        float* __restrict__ vscale) {
+  constexpr int EPL = D / 32;  // values per lane: 4 (d = 128) or 2 (d = 64)
+  const int row = blockIdx.x;
+  const int slot = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (slot >= k) return;  // whole warps leave together: the shuffles below see full warps
+  const int p = pos[static_cast<size_t>(row) * k + slot];
+  if (p < 0) return;
+  const size_t src = (static_cast<size_t>(row) * T + p) * D + lane * EPL;
+  const size_t dst = (static_cast<size_t>(row) * k + slot) * D + lane * EPL;
+#pragma unroll
+  for (int isv = 0; isv < 2; ++isv) {
+    const __nv_bfloat16* x = (isv ? V : K) + src;
+    float f[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) f[i] = __bfloat162float(x[i]);
+    uint32_t pairs[EPL / 2];
+    const float sc = quantize_e4m3<EPL>(f, 0xffffffffu, 32, pairs);
+    uint8_t* out = (isv ? Vc : Kc) + dst;
+    if constexpr (EPL == 4)
+      *reinterpret_cast<uint32_t*>(out) = pairs[0] | (pairs[1] << 16);
+    else
+      *reinterpret_cast<uint16_t*>(out) = static_cast<uint16_t>(pairs[0]);
+    if (lane == 0) (isv ? vscale : kscale)[static_cast<size_t>(row) * k + slot] = sc;
+  }
+}
+
 __global__ void reset_kernel(int rows, int k, float* __restrict__ score, int32_t* __restrict__ pos,
                              int32_t* __restrict__ meta) {
   const size_t n = static_cast<size_t>(rows) * k;
@@ -206,6 +242,22 @@ cudaError_t prefill_gather(const void* K, const void* V, int rows, int T, int d,
     gather_kernel<128><<<grid, 256, 0, stream>>>(kk, vv, T, k, pos, kc, vc);
   else
     gather_kernel<64><<<grid, 256, 0, stream>>>(kk, vv, T, k, pos, kc, vc);
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_gather_fp8(const void* K, const void* V, int rows, int T, int d, int k,
+                               const int32_t* pos, void* Kc, void* Vc, float* kscale,
+                               float* vscale, cudaStream_t stream) {
+  if (rows == 0 || T == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>((k + 7) / 8));
+  auto kk = static_cast<const __nv_bfloat16*>(K);
+  auto vv = static_cast<const __nv_bfloat16*>(V);
+  auto kc = static_cast<uint8_t*>(Kc);
+  auto vc = static_cast<uint8_t*>(Vc);
+  if (d == 128)
+    gather_fp8_kernel<128><<<grid, 256, 0, stream>>>(kk, vv, T, k, pos, kc, vc, kscale, vscale);
+  else
+    gather_fp8_kernel<64><<<grid, 256, 0, stream>>>(kk, vv, T, k, pos, kc, vc, kscale, vscale);
   return cudaGetLastError();
 }
 

@@ -54,6 +54,9 @@ extern "C" {
 #define H2O_MAX_T (1 << 20)  /* longest prompt accepted by h2o_prefill */
 #define H2O_MAX_K 32768      /* largest budget h + r accepted by h2o_create */
 
+#define H2O_KV_BF16 0  /* cache keys and values stored as bf16 (h2o_create) */
+#define H2O_KV_FP8 1   /* cache keys and values stored as E4M3 codes with per-token scales */
+
 typedef struct h2o_ctx h2o_ctx; /* opaque; created by h2o_create, freed by h2o_destroy */
 
 /*
@@ -62,7 +65,8 @@ typedef struct h2o_ctx h2o_ctx; /* opaque; created by h2o_create, freed by h2o_d
  * System Details: preallocated cache with a heavy-hitter and a recent region).
  *
  * Per layer the cache holds, for rows = batch * heads and k = h + r slots:
- *   K, V   bf16  [rows][k][d]   cached keys / values, slot-indexed
+ *   K, V   bf16  [rows][k][d]   cached keys / values, slot-indexed (E4M3
+ *                               codes, uint8, for an h2o_create_ex FP8 cache)
  *   score  fp32  [rows][k]      accumulated attention score of each slot
  *   pos    int32 [rows][k]      token position held by each slot (-1 = empty)
  *   meta   int32 [rows][4]      {filled slots, next position t, last evicted position (-1 none), 0}
@@ -73,6 +77,27 @@ typedef struct h2o_ctx h2o_ctx; /* opaque; created by h2o_create, freed by h2o_d
  * Errors: H2O_EINVAL, H2O_ENOMEM, H2O_ECUDA. On error *out is set to NULL.
  */
 int h2o_create(int layers, int batch, int heads, int head_dim, int h, int r, h2o_ctx** out);
+
+/*
+ * h2o_create_ex - h2o_create with a choice of cache storage. The pages report
+ * that H2O combines with quantisation of the KV cache and that the combination
+ * beats either alone ([H2O] 5, Empirical Evaluation), without fixing a scheme.
+ * kv_format H2O_KV_FP8 stores every cached token's key and value vectors as
+ * E4M3 codes (OCP 8-bit floating point: 1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits, largest finite value 448) with one fp32 scale per vector:
+ * scale = amax / 448 and code = E4M3(x * (448 / amax)), round to nearest even,
+ * saturated; a zero vector has scale 0. The arithmetic is fp32 with one
+ * rounding per operation. Prefill attention still runs on the full-precision
+ * prompt and the kept tokens are quantised as they enter the cache; a decode
+ * step quantises the new token first and attends to the stored (dequantised)
+ * values of every cached token, the new one included. Per layer the cache then
+ * holds K, V as uint8 [rows][k][d] and two fp32 [rows][k] scale arrays
+ * (h2o_cache_scales), 2d + 8 bytes per slot instead of 4d.
+ * kv_format H2O_KV_BF16 is h2o_create. Other arguments and errors as for
+ * h2o_create; an unknown kv_format gives H2O_EINVAL.
+ */
+int h2o_create_ex(int layers, int batch, int heads, int head_dim, int h, int r, int kv_format,
+                  h2o_ctx** out);
 
 /* h2o_destroy - free the cache and the context. Waits for the context's
  * stream work to finish first. NULL is accepted. */
@@ -195,6 +220,14 @@ int h2o_last_evicted(h2o_ctx* ctx, int layer, int32_t* host_pos);
  */
 int h2o_cache_view(h2o_ctx* ctx, int layer, void** K, void** V, float** score, int32_t** pos,
                    int32_t** meta);
+
+/*
+ * h2o_cache_scales - device addresses of one layer's per-slot scales of an
+ * H2O_KV_FP8 cache: k_scale, v_scale fp32 [rows][k] (a slot's stored key is
+ * E4M3(code) * k_scale). Same ownership and lifetime as h2o_cache_view; any
+ * output pointer may be NULL. Errors: H2O_EINVAL (also for a bf16 cache).
+ */
+int h2o_cache_scales(h2o_ctx* ctx, int layer, float** k_scale, float** v_scale);
 
 /* h2o_cache_dims - k (slots per row) and rows (batch * heads) per layer. */
 int h2o_cache_dims(h2o_ctx* ctx, int* k, int* rows);

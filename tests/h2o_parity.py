@@ -36,10 +36,11 @@ MEAN_ABS = 2e-3
 def _oracle_row(job):
     """Runs the oracle on one row; returns compact per-step logs (pool worker)."""
     os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
-    w, layer, b, j, row_block = job
+    w, layer, b, j, row_block, fp8 = job
     q, k, v = row_tokens(w, layer, b, j, head_direction(w, layer, j))
     q, k, v = bf16_bits_to_f64(q), bf16_bits_to_f64(k), bf16_bits_to_f64(v)
-    tr = oracle.run_row(q, k, v, w.prompt, w.steps, w.h, w.r, row_block=row_block)
+    tr = oracle.run_row(q, k, v, w.prompt, w.steps, w.h, w.r, row_block=row_block,
+                        kv_fp8_cache=fp8)
     pre = tr.prefill
     return {
         "O": pre.O.astype(np.float32),
@@ -56,8 +57,8 @@ def _oracle_row(job):
 
 
 def oracle_traces(w: Workload, layer: int, rows: list, workers: int | None = None,
-                  row_block: int | None = None) -> list:
-    jobs = [(w, layer, b, j, row_block) for (b, j) in rows]
+                  row_block: int | None = None, kv: str = "bf16") -> list:
+    jobs = [(w, layer, b, j, row_block, kv == "fp8") for (b, j) in rows]
     if workers is None:
         workers = min(len(jobs), max(1, (os.cpu_count() or 2) - 1))
     if workers <= 1 or len(jobs) <= 1:
@@ -76,6 +77,8 @@ class Report:
     near_ties: int = 0
     near_tie_mismatches: int = 0
     resyncs: int = 0
+    code_checks: int = 0  # FP8 cache: slots whose stored codes and scales were compared
+    code_mismatches: list = field(default_factory=list)
     prefill_max_abs: float = 0.0
     prefill_mean_abs: float = 0.0
     decode_max_abs: float = 0.0
@@ -83,7 +86,7 @@ class Report:
     score_max_rel: float = 0.0
 
     def ok(self) -> bool:
-        return (not self.mismatches and self.prefill_max_abs <= MAX_ABS
+        return (not self.mismatches and not self.code_mismatches and self.prefill_max_abs <= MAX_ABS
                 and self.prefill_mean_abs <= MEAN_ABS and self.decode_max_abs <= MAX_ABS
                 and self.decode_mean_abs <= MEAN_ABS)
 
@@ -92,10 +95,17 @@ def _to_bf16(bits: np.ndarray, device) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
 
 
+def _fp8_token(bits):
+    """The oracle's (codes, scale) of one bf16 token vector (FP8 cache)."""
+    return oracle.kv_fp8.quantize_vector(bf16_bits_to_f64(bits))
+
+
 def _resync_row(view, gpu_rows, pos: np.ndarray, scores: np.ndarray, k_bits, v_bits, k: int,
-                t_next: int):
+                t_next: int, scales=None):
     """Overwrite GPU rows (every copy of one checked row) with the oracle's
-    retained set, slots in ascending position order."""
+    retained set, slots in ascending position order (with ``scales``, the
+    views of an FP8 cache's scales, the tokens are stored as the oracle
+    quantises them)."""
     n = len(pos)
     dev = view["pos"].device
     rows_t = torch.as_tensor(np.atleast_1d(gpu_rows), device=dev, dtype=torch.long)
@@ -105,29 +115,62 @@ def _resync_row(view, gpu_rows, pos: np.ndarray, scores: np.ndarray, k_bits, v_b
     sc_full[:n] = scores
     view["pos"][rows_t] = torch.from_numpy(pos_full).to(dev)
     view["score"][rows_t] = torch.from_numpy(sc_full).to(dev)
-    kk = torch.zeros((k, k_bits.shape[1]), dtype=torch.bfloat16, device=dev)
-    vv = torch.zeros_like(kk)
-    if n:
-        kk[:n] = _to_bf16(k_bits[pos], dev)
-        vv[:n] = _to_bf16(v_bits[pos], dev)
-    view["K"][rows_t] = kk
-    view["V"][rows_t] = vv
+    if scales is not None:
+        kc = np.zeros((k, k_bits.shape[1]), dtype=np.uint8)
+        vc = np.zeros_like(kc)
+        ks = np.zeros(k, dtype=np.float32)
+        vs = np.zeros(k, dtype=np.float32)
+        for i, p_ in enumerate(pos):
+            kc[i], ks[i] = _fp8_token(k_bits[p_])
+            vc[i], vs[i] = _fp8_token(v_bits[p_])
+        view["K"][rows_t] = torch.from_numpy(kc).to(dev)
+        view["V"][rows_t] = torch.from_numpy(vc).to(dev)
+        scales["K"][rows_t] = torch.from_numpy(ks).to(dev)
+        scales["V"][rows_t] = torch.from_numpy(vs).to(dev)
+    else:
+        kk = torch.zeros((k, k_bits.shape[1]), dtype=torch.bfloat16, device=dev)
+        vv = torch.zeros_like(kk)
+        if n:
+            kk[:n] = _to_bf16(k_bits[pos], dev)
+            vv[:n] = _to_bf16(v_bits[pos], dev)
+        view["K"][rows_t] = kk
+        view["V"][rows_t] = vv
     view["meta"][rows_t] = torch.tensor([n, t_next, -1, 0], dtype=torch.int32, device=dev)
+
+
+def _check_codes(rep, view, scales, gpu_row, row_bits, max_slots=64):
+    """FP8 cache: every occupied slot of one GPU row must hold exactly the
+    oracle's codes and scales of the token at its position."""
+    pos = view["pos"][gpu_row].cpu().numpy()
+    kc, vc = view["K"][gpu_row].cpu().numpy(), view["V"][gpu_row].cpu().numpy()
+    ks, vs = scales["K"][gpu_row].cpu().numpy(), scales["V"][gpu_row].cpu().numpy()
+    _, kb, vb = row_bits
+    for slot in np.nonzero(pos >= 0)[0][:max_slots]:
+        p_ = int(pos[slot])
+        okc, oks = _fp8_token(kb[p_])
+        ovc, ovs = _fp8_token(vb[p_])
+        rep.code_checks += 1
+        if not (np.array_equal(kc[slot], okc) and np.array_equal(vc[slot], ovc)
+                and ks[slot] == oks and vs[slot] == ovs):
+            rep.code_mismatches.append((gpu_row, int(slot), p_))
 
 
 def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool = False,
                set_check_every: int = 1, workers: int | None = None,
-               row_block: int | None = None, traces: list | None = None) -> Report:
+               row_block: int | None = None, traces: list | None = None,
+               kv: str = "bf16") -> Report:
     """Runs one layer of workload ``w`` on the GPU and compares with the oracle.
 
-    ``rows``: (b, head) pairs checked against the oracle (default: all)."""
+    ``rows``: (b, head) pairs checked against the oracle (default: all).
+    ``kv``: cache storage, "bf16" or "fp8" (the oracle then runs its FP8 mode
+    and the stored codes and scales are compared bit for bit)."""
     import h2o_heavy_hitter_gb300 as h2o
 
     B, H, d, T, S, k = w.batch, w.heads, w.head_dim, w.prompt, w.steps, w.k
     if rows is None:
         rows = [(b, j) for b in range(B) for j in range(H)]
     if traces is None:
-        traces = oracle_traces(w, layer, rows, workers, row_block)
+        traces = oracle_traces(w, layer, rows, workers, row_block, kv)
     dev = torch.device("cuda")
     N = w.tokens
 
@@ -159,12 +202,17 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
         return np.nonzero(copies == ti)[0] if copies is not None else [g]
 
     rep = Report(rows=len(check), steps=S)
-    ctx = h2o.h2o_create(1, B, H, d, w.h, w.r)
+    fp8 = kv == "fp8"
+    ctx = h2o.h2o_create(1, B, H, d, w.h, w.r, kv=kv)
     try:
         out = h2o.h2o_prefill(ctx, 0, Qd[:, :, :T].contiguous(), Kd[:, :, :T].contiguous(),
                               Vd[:, :, :T].contiguous())
         view = h2o.h2o_cache_view(ctx, 0)
+        scales = h2o.h2o_cache_scales(ctx, 0) if fp8 else None
         gpu_rows = torch.tensor([g for g, _ in check], device=dev)
+        if fp8:
+            for g, ti in check[:8]:
+                _check_codes(rep, view, scales, g, row_bits[ti])
         O = out.reshape(B * H, T, d)[gpu_rows].cpu().numpy().astype(np.float64)
         errs = [np.abs(O[i] - traces[ti]["O"].astype(np.float64)) for i, (_, ti) in enumerate(check)]
         if T:
@@ -182,7 +230,8 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
                     rep.near_tie_mismatches += 1
                     rep.resyncs += 1
                     _, kb, vb = row_bits[ti]
-                    _resync_row(view, copies_of(g, ti), tr["kept"], tr["kept_scores"], kb, vb, k, T)
+                    _resync_row(view, copies_of(g, ti), tr["kept"], tr["kept_scores"], kb, vb, k, T,
+                                scales)
                 else:
                     rep.mismatches.append((-1, g, gp.tolist(), tr["kept"].tolist(), tr["margin"]))
             else:
@@ -228,7 +277,7 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
                         rep.resyncs += 1
                         _, kb, vb = row_bits[ti]
                         _resync_row(view, copies_of(g, ti), tr["kept_after"][s], tr["scores_after"][s],
-                                    kb, vb, k, T + s + 1)
+                                    kb, vb, k, T + s + 1, scales)
                         continue
                     rep.mismatches.append((s, g, int(ev[g]), int(tr["evicted"][s]), margin))
                     continue
@@ -246,6 +295,9 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
         if dcnt:
             rep.decode_max_abs = dmax
             rep.decode_mean_abs = dsum / dcnt
+        if fp8:  # the slots written by the decode steps
+            for g, ti in check[:8]:
+                _check_codes(rep, view, scales, g, row_bits[ti])
         h2o.h2o_sync_check(ctx)
     finally:
         ctx.close()

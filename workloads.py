@@ -164,13 +164,18 @@ def kv_cache_bytes(layers: int, hidden: int, batch: int, seq: int, bytes_per_ele
     return 2 * layers * hidden * batch * seq * bytes_per_elem
 
 
-def decode_bytes_per_row_step(k: int, d: int) -> int:
+def decode_bytes_per_row_step(k: int, d: int, kv: str = "bf16") -> int:
     """Algorithmic HBM bytes of one decode step of one (layer, b, head) row.
 
     Reads: the k cached K and V rows (bf16, 4kd), the k accumulated scores
     (fp32, 4k) and positions (int32, 4k), and q, k_new, v_new (bf16, 6d).
     Writes: the k updated scores (4k), the new slot's K/V (4d) with its
-    position and score (8), and the fp32 output (4d)."""
+    position and score (8), and the fp32 output (4d).
+    With an FP8 cache (kv="fp8") a slot holds E4M3 codes (2kd for K and V)
+    plus two fp32 scales (8k read), and the new slot is written as 2d code
+    bytes plus 8 scale bytes."""
+    if kv == "fp8":
+        return 2 * k * d + 8 * k + 12 * k + 6 * d + 2 * d + 16 + 4 * d
     return 4 * k * d + 12 * k + 6 * d + 4 * d + 8 + 4 * d
 
 
