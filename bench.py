@@ -334,23 +334,24 @@ def run_ours(args, w):
     # model layer would consume it); the last layer's values are the step's result.
     pre_out = torch.empty((B, H, T, d), dtype=torch.float32, device=dev)
     dec_out = torch.empty((S, B, H, d), dtype=torch.float32, device=dev)
-    h_pre_out = torch.empty(pre_out.shape, dtype=torch.float32).pin_memory()
-    h_dec_out = torch.empty(dec_out.shape, dtype=torch.float32).pin_memory()
 
     ctx = h2o.h2o_create(L, B, H, d, w.h, w.r, kv=args.kv)
     stream = torch.cuda.Stream(device=dev)
 
-    def prefill_all(c, layers):
+    def prefill_all(c, layers, prompt=None):
+        prompt = dp if prompt is None else prompt
         for layer in range(layers):
-            h2o.h2o_prefill(c, layer, *dp[layer % nl], out=pre_out)
+            h2o.h2o_prefill(c, layer, *prompt[layer % nl], out=pre_out)
 
-    def capture(c, layers, steps):
+    def capture(c, layers, steps, inputs=None, outs=None):
+        inputs = ds if inputs is None else inputs
+        outs = dec_out if outs is None else outs
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for s in range(steps):
                 for layer in range(layers):
-                    x = ds[layer % nl]
-                    h2o.h2o_decode_step(c, layer, x[0][s], x[1][s], x[2][s], dec_out[s])
+                    x = inputs[layer % nl]
+                    h2o.h2o_decode_step(c, layer, x[0][s], x[1][s], x[2][s], outs[s])
         return g
 
     torch.cuda.synchronize()
@@ -398,32 +399,63 @@ def run_ours(args, w):
     prefill_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     decode_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
 
-    # ---- end-to-end through the public API with host buffers
+    # ---- end to end through the public API with host buffers. Every step copies
+    # its inputs (the prompts and the decode steps' q, k, v) from pinned host
+    # memory and reads its result -- the decode outputs of the last layer --
+    # back into pinned host memory (the prefill's attention output would feed
+    # the next model layer on the device). Two device input sets and separate
+    # copy streams let step i's copies overlap the neighbouring steps' compute.
     h2d = sum(x.numel() * 2 for lay in hp + hs for x in lay)
-    d2h = (pre_out.numel() + dec_out.numel()) * 4
-
-    def e2e_step():
-        for dl, hl in zip(dp + ds, hp + hs):
-            for dst, src in zip(dl, hl):
-                dst.copy_(src, non_blocking=True)
-        step()
-        h_pre_out.copy_(pre_out, non_blocking=True)
-        h_dec_out.copy_(dec_out, non_blocking=True)
-
-    e2e_steps = max(3, args.steps // 4)
+    d2h = dec_out.numel() * 4
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    sets = [(dp, ds, dec_out, graph)]
+    dp2 = [[torch.empty_like(x) for x in lay] for lay in dp]
+    ds2 = [[torch.empty_like(x) for x in lay] for lay in ds]
+    out2 = torch.empty_like(dec_out)
     with torch.cuda.stream(stream):
-        e2e_step()
+        prefill_all(ctx, L, dp2)
+        sets.append((dp2, ds2, out2, capture(ctx, L, S, ds2, out2)))
+    h_out = [torch.empty(dec_out.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    copied = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    read = [torch.cuda.Event() for _ in range(2)]
+    torch.cuda.synchronize()
+
+    def e2e_step(i):
+        b = i % 2
+        pdev, sdev, odev, g_b = sets[b]
+        if i >= 2:
+            h2d_s.wait_event(done[b])  # step i - 2 no longer reads this input set
+        with torch.cuda.stream(h2d_s):
+            for dl, hl in zip(pdev + sdev, hp + hs):
+                for dst, src in zip(dl, hl):
+                    dst.copy_(src, non_blocking=True)
+            copied[b].record(h2d_s)
+        stream.wait_event(copied[b])
+        if i >= 2:
+            stream.wait_event(read[b])  # step i - 2's result has been read out
+        with torch.cuda.stream(stream):
+            prefill_all(ctx, L, pdev)
+            g_b.replay()
+            done[b].record(stream)
+        d2h_s.wait_event(done[b])
+        with torch.cuda.stream(d2h_s):
+            h_out[b].copy_(odev, non_blocking=True)
+            read[b].record(d2h_s)
+
+    e2e_steps = max(4, args.steps // 4)
+    for i in range(2):  # warm both input sets
+        e2e_step(i)
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
+    e0.record(h2d_s)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(d2h_s)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), pg, dev)
-    del graph
+    del graph, sets
 
     # ---- decode with the caches cycled through L2: when one layer's caches fit
     # in L2, a graph of decode steps over enough copies of the layer (more than
