@@ -510,7 +510,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 }
 
 // ------------------------------------------------------------------ column sums
-constexpr int kColThreads = 320;  // warps: 0 TMA, 1 MMA, 2-9 softmax (two per lane quadrant)
+constexpr int kColParts = 4;  // softmax warps per TMEM lane quadrant, each 128 / 4 query columns
+constexpr int kColCols = BM / kColParts;
+constexpr int kColWarps = 4 * kColParts;
+constexpr int kColThreads = (2 + kColWarps) * 32;  // warps: 0 TMA, 1 MMA, the rest softmax
 
 template <int D>
 struct ColCfg {
@@ -524,7 +527,7 @@ struct ColCfg {
   static constexpr uint32_t KA_COL = 256;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr size_t SMEM =
-      static_cast<size_t>(KST + QST) * TILE + LST * BM * sizeof(float) + 1024 + 4096;
+      static_cast<size_t>(KST + QST) * TILE + LST * BM * sizeof(float) + 1024 + 8192;
 };
 
 struct ColBars {
@@ -533,12 +536,12 @@ struct ColBars {
   uint64_t q_full[8], q_empty[8];
   uint64_t l_full[8], l_empty[8];
   uint64_t s_full[2], s_free[2];
-  uint64_t ebar[4];     // per lane quadrant, one phase per item: both halves' sums posted
-  float xsum[2][2][128];  // [item parity][half][key row]
+  uint64_t ebar[4];     // per lane quadrant, one phase per item: every part's sum posted
+  float xsum[2][kColParts][128];  // [item parity][part][key row]
   uint32_t tmem;
 };
 
-static_assert(sizeof(ColBars) <= 4096, "ColBars must fit the space reserved in ColCfg::SMEM");
+static_assert(sizeof(ColBars) <= 8192, "ColBars must fit the space reserved in ColCfg::SMEM");
 
 struct ColParams {
   const float* lse2;
@@ -572,10 +575,10 @@ __global__ void __launch_bounds__(kColThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->k_full[i], 1);
-      mbar_init(&bars->k_empty[i], 8);  // one arrival per softmax warp after its copy
-      mbar_init(&bars->ka_full[i], 8);
+      mbar_init(&bars->k_empty[i], kColWarps);  // one arrival per softmax warp after its copy
+      mbar_init(&bars->ka_full[i], kColWarps);
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_free[i], 8);
+      mbar_init(&bars->s_free[i], kColWarps);
     }
     for (int i = 0; i < C::QST; ++i) {
       mbar_init(&bars->q_full[i], 1);
@@ -583,9 +586,9 @@ __global__ void __launch_bounds__(kColThreads, 1)
     }
     for (int i = 0; i < C::LST; ++i) {
       mbar_init(&bars->l_full[i], 1);
-      mbar_init(&bars->l_empty[i], 8);
+      mbar_init(&bars->l_empty[i], kColWarps);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&bars->ebar[i], 2);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars->ebar[i], kColParts);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -678,24 +681,26 @@ __global__ void __launch_bounds__(kColThreads, 1)
       }
     }
   } else {
-    // Two warps per TMEM lane quadrant, one per half of the 128 query columns;
-    // a thread sums its key's probabilities over its half, and the halves are
-    // added once per item.
+    // kColParts warps per TMEM lane quadrant, each on kColCols of the 128 query
+    // columns; a thread sums its key's probabilities over its columns, and the
+    // parts are added once per item.
     const int sw = warp - 2;
-    const int quad = warp & 3, half = sw >> 2;
+    const int quad = warp & 3, part = sw >> 2;
     const int r = quad * 32 + lane;  // key row within the tile
-    const int cb = half * 64;        // first query column of this half
+    const int cb = part * kColCols;  // first query column of this part
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    // Copies this thread's key row, this warp's half of the channels (D/4
-    // bf16 pairs), from the staged key tile into TMEM buffer n & 1.
+    // Copies this thread's key row, this warp's part of the channels
+    // (D / (2 kColParts) bf16 pairs), from the staged key tile into TMEM
+    // buffer n & 1.
     auto copy_k = [&](int n) -> bool {
       const int ks = n & 1;
       if (!warp_wait(&bars->k_full[ks], (n >> 1) & 1, p.err)) return false;
       const uint8_t* tile = sK + ks * C::TILE;
-      uint32_t w[D / 4];
+      constexpr int CH = D / (8 * kColParts);  // 16-byte chunks of 8 channels per part
+      uint32_t w[4 * CH];
 #pragma unroll
-      for (int c = 0; c < D / 16; ++c) {  // 16-byte chunks of 8 channels
-        const int cg = half * (D / 16) + c;
+      for (int c = 0; c < CH; ++c) {
+        const int cg = part * CH + c;
         const uint4 v = *reinterpret_cast<const uint4*>(tile + (cg >> 3) * kBoxBytes + r * 128 +
                                                         (((cg & 7) ^ (r & 7)) << 4));
         w[4 * c] = v.x;
@@ -703,11 +708,11 @@ __global__ void __launch_bounds__(kColThreads, 1)
         w[4 * c + 2] = v.z;
         w[4 * c + 3] = v.w;
       }
-      const uint32_t dst = tmem + lane_off + C::KA_COL + (n & 1) * (D / 2) + half * (D / 4);
-      if constexpr (D == 128)
-        tmem_st32(dst, w);
-      else
+      const uint32_t dst = tmem + lane_off + C::KA_COL + (n & 1) * (D / 2) + part * (4 * CH);
+      if constexpr (4 * CH == 16)
         tmem_st16(dst, w);
+      else
+        tmem_st8(dst, w);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -733,9 +738,8 @@ __global__ void __launch_bounds__(kColThreads, 1)
           break;
         }
         tc_fence_after();
-        uint32_t s[64];
+        uint32_t s[kColCols];
         tmem_ld32(tmem + lane_off + sb * 128 + cb, s);
-        tmem_ld32(tmem + lane_off + sb * 128 + cb + 32, s + 32);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -752,10 +756,10 @@ __global__ void __launch_bounds__(kColThreads, 1)
         uint64_t a2[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) a2[e] = f2_pack(0.f, 0.f);
-        if (i == 0 || qvalid < 64) {
+        if (i == 0 || qvalid < kColCols) {
           const int c0 = i == 0 ? r - cb : 0;  // diagonal tile: queries >= key r only
 #pragma unroll
-          for (int c4 = 0; c4 < 64; c4 += 4) {
+          for (int c4 = 0; c4 < kColCols; c4 += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(L + c4);
             float x[4];
             f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c4]), __uint_as_float(s[c4 + 1])), sc2,
@@ -773,7 +777,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
           }
         } else {
 #pragma unroll
-          for (int c4 = 0; c4 < 64; c4 += 4) {
+          for (int c4 = 0; c4 < kColCols; c4 += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(L + c4);
             float x0, x1, x2, x3;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c4]), __uint_as_float(s[c4 + 1])), sc2,
@@ -794,14 +798,18 @@ __global__ void __launch_bounds__(kColThreads, 1)
         if (lane == 0) mbar_arrive(&bars->l_empty[ls]);
       }
       if (!ok) break;
-      // add the two halves
-      bars->xsum[j & 1][half][r] = acc;
+      // add the parts
+      bars->xsum[j & 1][part][r] = acc;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->ebar[quad]);
       if (!warp_wait(&bars->ebar[quad], j & 1, p.err)) break;
       const int key = kt * BN + r;
-      if (half == 0 && key < p.T)
-        p.colsum[static_cast<size_t>(row) * p.T + key] = acc + bars->xsum[j & 1][1][r];
+      if (part == 0 && key < p.T) {
+        float total = acc;
+#pragma unroll
+        for (int q = 1; q < kColParts; ++q) total += bars->xsum[j & 1][q][r];
+        p.colsum[static_cast<size_t>(row) * p.T + key] = total;
+      }
       g += nq;
     }
   }
