@@ -55,6 +55,7 @@ def load_library() -> ctypes.CDLL:
         "h2o_cache_scales": (I, [P, I, ctypes.POINTER(P), ctypes.POINTER(P)]),
         "h2o_destroy": (None, [P]),
         "h2o_prefill": (I, [P, I, P, P, P, I, P]),
+        "h2o_prefill_ragged": (I, [P, I, P, P, P, I, P, P]),
         "h2o_decode_step": (I, [P, I, P, P, P, P]),
         "h2o_prefill_attention": (I, [P, P, P, I, I, I, P, P]),
         "h2o_cache_positions": (I, [P, I, I32P]),
@@ -150,8 +151,13 @@ def h2o_destroy(ctx: H2OContext) -> None:
     ctx.close()
 
 
-def h2o_prefill(ctx: H2OContext, layer: int, Q, K, V, out=None) -> torch.Tensor:
-    """Prompt pass of one layer; returns the fp32 attention output [B, H, T, d]."""
+def h2o_prefill(ctx: H2OContext, layer: int, Q, K, V, out=None, lens=None) -> torch.Tensor:
+    """Prompt pass of one layer; returns the fp32 attention output [B, H, T, d].
+
+    ``lens``: for a ragged batch, a CUDA int32 tensor [B] of prompt lengths
+    (h2o_prefill_ragged); Q, K, V then hold each prompt right-padded to
+    T = Q.shape[2] with finite padding, and output rows past a prompt's length
+    hold no result."""
     T = Q.shape[2] if Q is not None and Q.dim() == 4 else 0
     shape = (ctx.batch, ctx.heads, T, ctx.head_dim)
     if out is None:
@@ -160,7 +166,12 @@ def h2o_prefill(ctx: H2OContext, layer: int, Q, K, V, out=None) -> torch.Tensor:
     pk = _dev_ptr(K, torch.bfloat16, shape, "K")
     pv = _dev_ptr(V, torch.bfloat16, shape, "V")
     po = _dev_ptr(out, torch.float32, shape, "out")
-    _check(load_library().h2o_prefill(ctypes.c_void_p(ctx.handle), layer, pq, pk, pv, T, po))
+    lib = load_library()
+    if lens is None:
+        _check(lib.h2o_prefill(ctypes.c_void_p(ctx.handle), layer, pq, pk, pv, T, po))
+    else:
+        pl = _dev_ptr(lens, torch.int32, (ctx.batch,), "lens")
+        _check(lib.h2o_prefill_ragged(ctypes.c_void_p(ctx.handle), layer, pq, pk, pv, T, pl, po))
     return out
 
 

@@ -13,7 +13,18 @@ namespace h2o {
 enum DeviceError : int {
   kErrWaitTimeout = 1,  // an mbarrier wait gave up
   kErrBadState = 2,     // a kernel found inconsistent row metadata
+  kErrBadLength = 4,    // a ragged batch's prompt length was outside [0, T_max]
 };
+
+// Prompt length of `row` (= batch * heads + head) in a prefill launch over
+// prompts padded to T tokens: T, or the length of the row's batch entry when
+// per-entry lengths are given, clamped to [0, T] so that no access leaves the
+// padded tensors (the selection kernel reports lengths out of range).
+__device__ __forceinline__ int row_len(const int32_t* lens, int heads, int row, int T) {
+  if (!lens) return T;
+  const int n = lens[row / heads];
+  return n < 0 ? 0 : (n > T ? T : n);
+}
 
 // Wall-clock bound of every device-side wait, in nanoseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;

@@ -107,13 +107,56 @@ int check_layer(const h2o_ctx* c, int layer) {
   return H2O_OK;
 }
 
-int run_attention(const void* Q, const void* K, const void* V, int rows, int T, int d, float* out,
-                  float* colsum, int32_t* err, cudaStream_t s) {
+int run_attention(const void* Q, const void* K, const void* V, int rows, int T,
+                  const int32_t* lens, int heads, int d, float* out, float* colsum, int32_t* err,
+                  cudaStream_t s) {
   Scratch lse(static_cast<size_t>(rows) * h2o::lse_stride(T) * sizeof(float), s);
-  cudaError_t e = h2o::prefill_forward(Q, K, V, rows, T, d, out, static_cast<float*>(lse.p), err, s);
+  cudaError_t e = h2o::prefill_forward(Q, K, V, rows, T, lens, heads, d, out,
+                                       static_cast<float*>(lse.p), err, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefill forward launch");
-  e = h2o::prefill_colsum(Q, K, static_cast<float*>(lse.p), rows, T, d, colsum, err, s);
+  e = h2o::prefill_colsum(Q, K, static_cast<float*>(lse.p), rows, T, lens, heads, d, colsum, err, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefill column-sum launch");
+  return H2O_OK;
+}
+
+// Prefill of one layer over prompts padded to T tokens; `lens` (device, one
+// length per batch entry) or null for prompts of exactly T tokens.
+int prefill_layer(h2o_ctx* c, int layer, const void* Q, const void* K, const void* V, int T,
+                  const int32_t* lens, float* out) {
+  if (int rc = check_layer(c, layer)) return rc;
+  if (T < 0 || T > H2O_MAX_T) return fail(H2O_EINVAL, "T out of range");
+  cudaStream_t s = current_stream();
+  cudaError_t e;
+  if (T == 0) {
+    e = h2o::cache_reset(c->rows, c->k, c->layer_score(layer), c->layer_pos(layer),
+                         c->layer_meta(layer), s);
+    if (e != cudaSuccess) return cuda_fail(e, "cache reset");
+    c->prompt_len[layer] = 0;
+    return H2O_OK;
+  }
+  if (!Q || !K || !V || !out) return fail(H2O_EINVAL, "null Q, K, V or out");
+  if (!tma_aligned(Q, K, V, out)) return fail(H2O_EINVAL, "Q, K, V and out must be 16-byte aligned");
+  const int heads = c->heads;
+  try {
+    Scratch colsum(static_cast<size_t>(c->rows) * T * sizeof(float), s);
+    int rc = run_attention(Q, K, V, c->rows, T, lens, heads, c->d, out,
+                           static_cast<float*>(colsum.p), c->err, s);
+    if (rc) return rc;
+    e = h2o::prefill_select(static_cast<float*>(colsum.p), c->rows, T, lens, heads, c->h, c->r,
+                            c->layer_score(layer), c->layer_pos(layer), c->layer_meta(layer),
+                            c->err, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill select launch");
+    e = c->kv_format == H2O_KV_FP8
+            ? h2o::prefill_gather_fp8(K, V, c->rows, T, c->d, c->k, c->layer_pos(layer),
+                                      c->layer_K(layer), c->layer_V(layer),
+                                      c->layer_kscale(layer), c->layer_vscale(layer), s)
+            : h2o::prefill_gather(K, V, c->rows, T, c->d, c->k, c->layer_pos(layer),
+                                  c->layer_K(layer), c->layer_V(layer), s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill gather launch");
+  } catch (const std::exception& ex) {
+    return fail(H2O_ENOMEM, std::string("prefill scratch allocation failed: ") + ex.what());
+  }
+  c->prompt_len[layer] = T;
   return H2O_OK;
 }
 
@@ -237,38 +280,13 @@ void h2o_destroy(h2o_ctx* c) {
 
 int h2o_prefill(h2o_ctx* c, int layer, const void* Q, const void* K, const void* V, int T,
                 float* out) {
-  if (int rc = check_layer(c, layer)) return rc;
-  if (T < 0 || T > H2O_MAX_T) return fail(H2O_EINVAL, "T out of range");
-  cudaStream_t s = current_stream();
-  cudaError_t e;
-  if (T == 0) {
-    e = h2o::cache_reset(c->rows, c->k, c->layer_score(layer), c->layer_pos(layer),
-                         c->layer_meta(layer), s);
-    if (e != cudaSuccess) return cuda_fail(e, "cache reset");
-    c->prompt_len[layer] = 0;
-    return H2O_OK;
-  }
-  if (!Q || !K || !V || !out) return fail(H2O_EINVAL, "null Q, K, V or out");
-  if (!tma_aligned(Q, K, V, out)) return fail(H2O_EINVAL, "Q, K, V and out must be 16-byte aligned");
-  try {
-    Scratch colsum(static_cast<size_t>(c->rows) * T * sizeof(float), s);
-    int rc = run_attention(Q, K, V, c->rows, T, c->d, out, static_cast<float*>(colsum.p), c->err, s);
-    if (rc) return rc;
-    e = h2o::prefill_select(static_cast<float*>(colsum.p), c->rows, T, c->h, c->r,
-                            c->layer_score(layer), c->layer_pos(layer), c->layer_meta(layer), s);
-    if (e != cudaSuccess) return cuda_fail(e, "prefill select launch");
-    e = c->kv_format == H2O_KV_FP8
-            ? h2o::prefill_gather_fp8(K, V, c->rows, T, c->d, c->k, c->layer_pos(layer),
-                                      c->layer_K(layer), c->layer_V(layer),
-                                      c->layer_kscale(layer), c->layer_vscale(layer), s)
-            : h2o::prefill_gather(K, V, c->rows, T, c->d, c->k, c->layer_pos(layer),
-                                  c->layer_K(layer), c->layer_V(layer), s);
-    if (e != cudaSuccess) return cuda_fail(e, "prefill gather launch");
-  } catch (const std::exception& ex) {
-    return fail(H2O_ENOMEM, std::string("prefill scratch allocation failed: ") + ex.what());
-  }
-  c->prompt_len[layer] = T;
-  return H2O_OK;
+  return prefill_layer(c, layer, Q, K, V, T, nullptr, out);
+}
+
+int h2o_prefill_ragged(h2o_ctx* c, int layer, const void* Q, const void* K, const void* V,
+                       int T_max, const int32_t* lens, float* out) {
+  if (T_max > 0 && !lens) return fail(H2O_EINVAL, "null lens");
+  return prefill_layer(c, layer, Q, K, V, T_max, lens, out);
 }
 
 int h2o_prefill_attention(const void* Q, const void* K, const void* V, int rows, int T,
@@ -279,7 +297,8 @@ int h2o_prefill_attention(const void* Q, const void* K, const void* V, int rows,
   if (!Q || !K || !V || !out || !score) return fail(H2O_EINVAL, "null pointer");
   if (!tma_aligned(Q, K, V, out)) return fail(H2O_EINVAL, "Q, K, V and out must be 16-byte aligned");
   try {
-    return run_attention(Q, K, V, rows, T, head_dim, out, score, nullptr, current_stream());
+    return run_attention(Q, K, V, rows, T, nullptr, 1, head_dim, out, score, nullptr,
+                         current_stream());
   } catch (const std::exception& ex) {
     return fail(H2O_ENOMEM, std::string("scratch allocation failed: ") + ex.what());
   }
@@ -301,9 +320,9 @@ int h2o_prefill_attention_noalloc(const void* Q, const void* K, const void* V, i
   cudaError_t e = h2o::noalloc_lse_scratch(&lse);
   if (e != cudaSuccess) return cuda_fail(e, "scratch address lookup");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  e = h2o::prefill_forward(Q, K, V, rows, T, head_dim, out, lse, nullptr, s);
+  e = h2o::prefill_forward(Q, K, V, rows, T, nullptr, 1, head_dim, out, lse, nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefill forward launch");
-  e = h2o::prefill_colsum(Q, K, lse, rows, T, head_dim, score, nullptr, s);
+  e = h2o::prefill_colsum(Q, K, lse, rows, T, nullptr, 1, head_dim, score, nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefill column-sum launch");
   return H2O_OK;
 }
@@ -395,8 +414,8 @@ int h2o_sync_check(h2o_ctx* c) {
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
   if (word != 0) {
     cudaMemsetAsync(c->err, 0, sizeof(int32_t), s);
-    char buf[96];
-    std::snprintf(buf, sizeof(buf), "device error word 0x%x (1 = wait timeout, 2 = bad state)", word);
+    char buf[128];
+    std::snprintf(buf, sizeof(buf), "device error word 0x%x (1 = wait timeout, 2 = bad state, 4 = length out of range)", word);
     return fail(H2O_EDEVICE, buf);
   }
   return H2O_OK;

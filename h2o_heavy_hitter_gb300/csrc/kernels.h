@@ -66,20 +66,29 @@ inline int lse_stride(int T) { return (T + 127) / 128 * 128; }
 
 // Causal attention over `rows` rows of T tokens: O (fp32 [rows][T][d]) and the
 // negated base-2 log-sum-exp of each query row's scaled logits, -lse2
-// (fp32 [rows][lse_stride(T)]).
-cudaError_t prefill_forward(const void* Q, const void* K, const void* V, int rows, int T, int d,
-                            float* O, float* lse2, int32_t* err, cudaStream_t stream);
+// (fp32 [rows][lse_stride(T)]). Ragged batch: with `lens` (device int32, one
+// length per batch entry of `heads` rows) row i holds a prompt of
+// lens[i / heads] tokens padded to T; results past a row's length are not
+// written (O rows of the last 32-token box may be) and the padding of Q, K, V
+// must be finite (padded keys enter the MMAs with probability 0).
+cudaError_t prefill_forward(const void* Q, const void* K, const void* V, int rows, int T,
+                            const int32_t* lens, int heads, int d, float* O, float* lse2,
+                            int32_t* err, cudaStream_t stream);
 // Column sums of the causal probability matrix (fp32 [rows][T]), given -lse2.
 cudaError_t prefill_colsum(const void* Q, const void* K, const float* lse2, int rows, int T,
-                           int d, float* colsum, int32_t* err, cudaStream_t stream);
+                           const int32_t* lens, int heads, int d, float* colsum, int32_t* err,
+                           cudaStream_t stream);
 // Device address of the library's fixed log-sum-exp array used by
 // h2o_prefill_attention_noalloc (H2O_NOALLOC_MAX_LSE floats). Looked up once
 // per device, with that device current, and cached.
 cudaError_t noalloc_lse_scratch(float** out);
 
-// Top-h plus recent selection of every row into the cache's pos/score/meta.
-cudaError_t prefill_select(const float* colsum, int rows, int T, int h, int r, float* score,
-                           int32_t* pos, int32_t* meta, cudaStream_t stream);
+// Top-h plus recent selection of every row into the cache's pos/score/meta
+// (colsum rows T floats apart; per-row lengths as for prefill_forward; a
+// length outside [0, T] is clamped and sets kErrBadLength in *err).
+cudaError_t prefill_select(const float* colsum, int rows, int T, const int32_t* lens, int heads,
+                           int h, int r, float* score, int32_t* pos, int32_t* meta, int32_t* err,
+                           cudaStream_t stream);
 // Copies the selected prompt K/V rows into the cache slots.
 cudaError_t prefill_gather(const void* K, const void* V, int rows, int T, int d, int k,
                            const int32_t* pos, void* Kc, void* Vc, cudaStream_t stream);

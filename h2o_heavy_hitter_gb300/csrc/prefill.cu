@@ -114,7 +114,9 @@ static_assert(sizeof(FwdBars) <= 2048, "FwdBars must fit the space reserved in F
 
 struct FwdParams {
   float* lse2;
-  int rows, T, Tp, nqt, nqb, items;  // nqb = blocks of two query tiles per row
+  const int32_t* lens;  // per batch entry prompt lengths (ragged batch) or null
+  int heads;            // rows per batch entry (row / heads indexes lens)
+  int rows, T, Tp, nqt, nqb, items;  // T padded length; nqb = blocks of two query tiles per row
   int rb;  // rows per L2 block of the item order
   float qscale;
   int32_t* err;
@@ -233,12 +235,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const CUtensorMap* map = is_k ? &tk : &tv;
       uint32_t g = 0;
       bool ok = true;
-      int j = 0;
-      for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x, ++j) {
+      int j = 0;  // items processed (query loads)
+      for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x) {
         int row, rank;
         item_coords(it, p.rows, p.nqb, p.rb, row, rank);
+        const int nqt = (row_len(p.lens, p.heads, row, p.T) + BM - 1) / BM;
         const int qa = 2 * (p.nqb - 1 - rank);
-        const bool has_b = qa + 1 < p.nqt;
+        if (qa >= nqt) continue;  // past the end of this row's prompt
+        const bool has_b = qa + 1 < nqt;
         const int nk = has_b ? qa + 2 : qa + 1;
         if (is_k) {
           if (j > 0 && !mbar_wait(&bars->q_empty, (j - 1) & 1, p.err)) break;  // last S done
@@ -256,6 +260,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mbar_arrive_expect_tx(&full[st], C::TILE);
           load_tile<D>(ring + st * C::TILE, map, kt, row, &full[st]);
         }
+        ++j;
       }
     }
   } else if (warp == kWarpMMA) {
@@ -290,11 +295,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           umma_ss(d_tm, qb + off, kb + off, idesc_qk, kk > 0);
         }
       };
-      for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x, ++j) {
+      for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x) {
         int row, rank;
         item_coords(it, p.rows, p.nqb, p.rb, row, rank);
+        const int nqt = (row_len(p.lens, p.heads, row, p.T) + BM - 1) / BM;
         const int qa = 2 * (p.nqb - 1 - rank);
-        const bool has_b = qa + 1 < p.nqt;
+        if (qa >= nqt) continue;
+        const bool has_b = qa + 1 < nqt;
         const int nk = has_b ? qa + 2 : qa + 1;
         const int last_a = qa, last_b = qa + 1;
         if (!mbar_wait(&bars->q_full, j & 1, p.err)) break;
@@ -361,6 +368,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           n1 += last_b + 1;
           ++e1;
         }
+        ++j;
       }
     }
   } else {
@@ -379,8 +387,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     for (int it = blockIdx.x; ok && it < p.items; it += gridDim.x) {
       int row, rank;
       item_coords(it, p.rows, p.nqb, p.rb, row, rank);
+      const int tlen = row_len(p.lens, p.heads, row, p.T);
       const int qt = 2 * (p.nqb - 1 - rank) + t;
-      if (qt >= p.nqt) continue;  // tile B of a ragged last block: nothing to do
+      if (qt * BM >= tlen) continue;  // past the prompt (tile B of a last block, or a short row)
       const int qrow = qt * BM + r;
       float m = -INFINITY, l = 0.f;
       for (int kt = 0; kt <= qt; ++kt) {
@@ -476,7 +485,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->o_free[t]);
       const float inv = 1.f / l;
-      if (qrow < p.T) p.lse2[static_cast<size_t>(row) * p.Tp + qrow] = -(m + log2f(l));
+      if (qrow < tlen) p.lse2[static_cast<size_t>(row) * p.Tp + qrow] = -(m + log2f(l));
       const int tok0 = qt * BM + quad * 32;  // first token of this warp's rows
 #pragma unroll
       for (int c = 0; c < D / 16; ++c, ++rounds) {
@@ -492,7 +501,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          if (tok0 < p.T) tma_store_3d(&to, stg, c * 16, tok0, row);  // rows past T are clipped
+          // rows past the padded length are clipped; rows of the last box past
+          // a shorter row's prompt land in its padding, which holds no result
+          if (tok0 < tlen) tma_store_3d(&to, stg, c * 16, tok0, row);
           bulk_commit();
         }
       }
@@ -546,7 +557,9 @@ static_assert(sizeof(ColBars) <= 8192, "ColBars must fit the space reserved in C
 struct ColParams {
   const float* lse2;
   float* colsum;
-  int rows, T, Tp, nqt, items;
+  const int32_t* lens;  // per batch entry prompt lengths (ragged batch) or null
+  int heads;            // rows per batch entry
+  int rows, T, Tp, nqt, items;  // T padded length
   int rb;  // rows per L2 block of the item order
   float qscale;
   int32_t* err;
@@ -624,7 +637,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
       for (int j = 0; ok && j < n_items; ++j) {
         int row, kt;
         item_coords(blockIdx.x + j * gridDim.x, p.rows, p.nqt, p.rb, row, kt);
-        const int nq = p.nqt - kt;
+        const int nq = max(0, (row_len(p.lens, p.heads, row, p.T) + BM - 1) / BM - kt);
         for (int i = 0; i < nq; ++i, ++g) {
           const int st = g % C::QST, ls = g % C::LST, qt = kt + i;
           if (g >= C::QST && !mbar_wait(&bars->q_empty[st], ((g / C::QST) - 1) & 1, p.err)) {
@@ -654,7 +667,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
       for (int j = 0; j < n_items; ++j) {
         int row, kt;
         item_coords(blockIdx.x + j * gridDim.x, p.rows, p.nqt, p.rb, row, kt);
-        const int nq = p.nqt - kt;
+        const int nq = max(0, (row_len(p.lens, p.heads, row, p.T) + BM - 1) / BM - kt);
         const int kb = j & 1;
         if (!mbar_wait(&bars->ka_full[kb], (j >> 1) & 1, p.err)) break;
         bool ok = true;
@@ -727,7 +740,10 @@ __global__ void __launch_bounds__(kColThreads, 1)
     for (int j = 0; ok && j < n_items; ++j) {
       int row, kt;
       item_coords(blockIdx.x + j * gridDim.x, p.rows, p.nqt, p.rb, row, kt);
-      const int nq = p.nqt - kt;
+      const int tlen = row_len(p.lens, p.heads, row, p.T);
+      // items past a short row's prompt have no queries: the key tile still
+      // passes through TMEM so that every barrier phase stays in step
+      const int nq = max(0, (tlen + BM - 1) / BM - kt);
       if (j + 1 < n_items && !copy_k(j + 1)) break;
       float acc = 0.f;
       for (int i = 0; i < nq; ++i) {
@@ -749,7 +765,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
           break;
         }
         const float* L = sL + ls * BM + cb;
-        const int qvalid = min(BM, p.T - qt * BM) - cb;  // queries past the prompt end are padding
+        const int qvalid = min(BM, tlen - qt * BM) - cb;  // queries past the prompt end are padding
         // L holds -lse2 of each query: p = 2^(s * qscale - lse2), two queries per
         // packed fma / add; the LSE values come as float4 loads.
         const uint64_t sc2 = f2_pack(p.qscale, p.qscale);
@@ -804,7 +820,7 @@ __global__ void __launch_bounds__(kColThreads, 1)
       if (lane == 0) mbar_arrive(&bars->ebar[quad]);
       if (!warp_wait(&bars->ebar[quad], j & 1, p.err)) break;
       const int key = kt * BN + r;
-      if (part == 0 && key < p.T) {
+      if (part == 0 && key < tlen) {
         float total = acc;
 #pragma unroll
         for (int q = 1; q < kColParts; ++q) total += bars->xsum[j & 1][q][r];
@@ -886,8 +902,9 @@ cudaError_t make_store_map(CUtensorMap* m, void* base, int rows, int T, int D) {
 }
 
 template <int D>
-cudaError_t forward_t(const void* Q, const void* K, const void* V, int rows, int T, float* O,
-                      float* lse2, int32_t* err, cudaStream_t stream) {
+cudaError_t forward_t(const void* Q, const void* K, const void* V, int rows, int T,
+                      const int32_t* lens, int heads, float* O, float* lse2, int32_t* err,
+                      cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mo;
   cudaError_t e;
   if ((e = make_map(&mq, Q, rows, T, D)) != cudaSuccess) return e;
@@ -902,8 +919,8 @@ cudaError_t forward_t(const void* Q, const void* K, const void* V, int rows, int
     attr = true;
   }
   const int nqt = (T + BM - 1) / BM, nqb = (nqt + 1) / 2;
-  FwdParams p{lse2, rows, T, lse_stride(T), nqt, nqb, rows * nqb, rows_per_l2_block(T, D, 2),
-              kLog2e / sqrtf(float(D)), err};
+  FwdParams p{lse2, lens, heads, rows, T, lse_stride(T), nqt, nqb, rows * nqb,
+              rows_per_l2_block(T, D, 2), kLog2e / sqrtf(float(D)), err};
   const unsigned grid = static_cast<unsigned>(std::min(p.items, num_sms()));
   attn_fwd_kernel<D><<<grid, kFwdThreads, FwdCfg<D>::SMEM, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
@@ -911,7 +928,8 @@ cudaError_t forward_t(const void* Q, const void* K, const void* V, int rows, int
 
 template <int D>
 cudaError_t colsum_t(const void* Q, const void* K, const float* lse2, int rows, int T,
-                     float* colsum, int32_t* err, cudaStream_t stream) {
+                     const int32_t* lens, int heads, float* colsum, int32_t* err,
+                     cudaStream_t stream) {
   CUtensorMap mq, mk;
   cudaError_t e;
   if ((e = make_map(&mq, Q, rows, T, D)) != cudaSuccess) return e;
@@ -924,8 +942,8 @@ cudaError_t colsum_t(const void* Q, const void* K, const float* lse2, int rows, 
     attr = true;
   }
   const int nqt = (T + BM - 1) / BM;
-  ColParams p{lse2, colsum, rows, T, lse_stride(T), nqt, rows * nqt, rows_per_l2_block(T, D, 1),
-              kLog2e / sqrtf(float(D)), err};
+  ColParams p{lse2, colsum, lens, heads, rows, T, lse_stride(T), nqt, rows * nqt,
+              rows_per_l2_block(T, D, 1), kLog2e / sqrtf(float(D)), err};
   const unsigned grid = static_cast<unsigned>(std::min(p.items, num_sms()));
   attn_colsum_kernel<D><<<grid, kColThreads, ColCfg<D>::SMEM, stream>>>(mq, mk, p);
   return cudaGetLastError();
@@ -933,18 +951,20 @@ cudaError_t colsum_t(const void* Q, const void* K, const float* lse2, int rows, 
 
 }  // namespace
 
-cudaError_t prefill_forward(const void* Q, const void* K, const void* V, int rows, int T, int d,
-                            float* O, float* lse2, int32_t* err, cudaStream_t stream) {
+cudaError_t prefill_forward(const void* Q, const void* K, const void* V, int rows, int T,
+                            const int32_t* lens, int heads, int d, float* O, float* lse2,
+                            int32_t* err, cudaStream_t stream) {
   if (static_cast<long>(rows) * T == 0) return cudaSuccess;
-  return d == 128 ? forward_t<128>(Q, K, V, rows, T, O, lse2, err, stream)
-                  : forward_t<64>(Q, K, V, rows, T, O, lse2, err, stream);
+  return d == 128 ? forward_t<128>(Q, K, V, rows, T, lens, heads, O, lse2, err, stream)
+                  : forward_t<64>(Q, K, V, rows, T, lens, heads, O, lse2, err, stream);
 }
 
 cudaError_t prefill_colsum(const void* Q, const void* K, const float* lse2, int rows, int T,
-                           int d, float* colsum, int32_t* err, cudaStream_t stream) {
+                           const int32_t* lens, int heads, int d, float* colsum, int32_t* err,
+                           cudaStream_t stream) {
   if (static_cast<long>(rows) * T == 0) return cudaSuccess;
-  return d == 128 ? colsum_t<128>(Q, K, lse2, rows, T, colsum, err, stream)
-                  : colsum_t<64>(Q, K, lse2, rows, T, colsum, err, stream);
+  return d == 128 ? colsum_t<128>(Q, K, lse2, rows, T, lens, heads, colsum, err, stream)
+                  : colsum_t<64>(Q, K, lse2, rows, T, lens, heads, colsum, err, stream);
 }
 
 // ------------------------------------------------------------------ allocation-free scratch

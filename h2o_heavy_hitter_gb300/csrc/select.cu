@@ -49,17 +49,25 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int* wsum, int* total
   return r;
 }
 
+// colsum rows are `stride` floats apart (the padded prompt length); the row's
+// own prompt length T is `stride`, or its batch entry's length in `lens`.
 __global__ void __launch_bounds__(kSelectThreads) select_kernel(const float* __restrict__ colsum,
-                                                               int T, int h, int r, int k,
+                                                               int stride,
+                                                               const int32_t* __restrict__ lens,
+                                                               int heads, int h, int r, int k,
                                                                float* __restrict__ score,
                                                                int32_t* __restrict__ pos,
-                                                               int32_t* __restrict__ meta) {
+                                                               int32_t* __restrict__ meta,
+                                                               int32_t* __restrict__ err) {
   __shared__ unsigned hist[256];
   __shared__ int wsum[33];
   __shared__ unsigned s_prefix;
   __shared__ int s_rank;
   const int row = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
-  const float* cs = colsum + static_cast<size_t>(row) * T;
+  const int T = row_len(lens, heads, row, stride);
+  if (lens && tid == 0 && row % heads == 0 && T != lens[row / heads] && err)
+    atomicOr(err, kErrBadLength);
+  const float* cs = colsum + static_cast<size_t>(row) * stride;
   float* sc = score + static_cast<size_t>(row) * k;
   int32_t* ps = pos + static_cast<size_t>(row) * k;
 
@@ -223,10 +231,12 @@ __global__ void reset_kernel(int rows, int k, float* __restrict__ score, int32_t
 
 }  // namespace
 
-cudaError_t prefill_select(const float* colsum, int rows, int T, int h, int r, float* score,
-                           int32_t* pos, int32_t* meta, cudaStream_t stream) {
+cudaError_t prefill_select(const float* colsum, int rows, int T, const int32_t* lens, int heads,
+                           int h, int r, float* score, int32_t* pos, int32_t* meta, int32_t* err,
+                           cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  select_kernel<<<rows, kSelectThreads, 0, stream>>>(colsum, T, h, r, h + r, score, pos, meta);
+  select_kernel<<<rows, kSelectThreads, 0, stream>>>(colsum, T, lens, heads, h, r, h + r, score,
+                                                     pos, meta, err);
   return cudaGetLastError();
 }
 

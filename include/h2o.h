@@ -125,6 +125,34 @@ int h2o_prefill(h2o_ctx* ctx, int layer, const void* Q, const void* K, const voi
                 float* out);
 
 /*
+ * h2o_prefill_ragged - h2o_prefill of a batch whose prompts differ in length
+ * ([H2O] 5, Empirical Evaluation, Throughput and Latency: the gains come from
+ * serving larger batches; entries of a batch are independent sequences, and
+ * their prompts need not be equally long).
+ *
+ * Batch entry b holds a prompt of T_b = lens[b] tokens, stored right-padded
+ * to T_max: Q, K, V device bf16 [batch, heads, T_max, d] with token t of entry
+ * b at index t for t < T_b. Each row is processed exactly as h2o_prefill
+ * processes a prompt of T_b tokens (attention, column sums, the r most recent
+ * tokens T_b - r .. T_b - 1 plus the top-h others, or all T_b tokens when
+ * T_b <= h + r), and its first decode step then processes position T_b.
+ *
+ * lens: device int32 [batch], 0 <= lens[b] <= T_max, read on the device (the
+ * call can be captured in a CUDA graph with lengths written later). A length
+ * outside that range is clamped into it and sets bit 4 of the device error
+ * word (h2o_sync_check reports H2O_EDEVICE). The padding tokens t >= T_b of
+ * Q, K and V must hold finite values (zeros, say): padded keys and values
+ * enter the tensor-core products with probability 0, and 0 times a non-finite
+ * value is not 0. out: device fp32 [batch, heads, T_max, d]; rows t >= T_b
+ * hold no result (the call may write them). Scratch as for h2o_prefill, sized
+ * by T_max. With T_max = 0 the pointers may be NULL and every row is reset to
+ * an empty cache. Errors: H2O_EINVAL (also for lens NULL with T_max > 0),
+ * H2O_ENOMEM, H2O_ECUDA.
+ */
+int h2o_prefill_ragged(h2o_ctx* ctx, int layer, const void* Q, const void* K, const void* V,
+                       int T_max, const int32_t* lens, float* out);
+
+/*
  * h2o_decode_step - one generation step of one layer ([H2O] 4.1 and 2).
  *
  * For every row, with t its next position: append the new token (q, k_new,

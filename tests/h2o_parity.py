@@ -36,10 +36,10 @@ MEAN_ABS = 2e-3
 def _oracle_row(job):
     """Runs the oracle on one row; returns compact per-step logs (pool worker)."""
     os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
-    w, layer, b, j, row_block, fp8 = job
+    w, layer, b, j, row_block, fp8, prompt = job
     q, k, v = row_tokens(w, layer, b, j, head_direction(w, layer, j))
     q, k, v = bf16_bits_to_f64(q), bf16_bits_to_f64(k), bf16_bits_to_f64(v)
-    tr = oracle.run_row(q, k, v, w.prompt, w.steps, w.h, w.r, row_block=row_block,
+    tr = oracle.run_row(q, k, v, prompt, w.steps, w.h, w.r, row_block=row_block,
                         kv_fp8_cache=fp8)
     pre = tr.prefill
     return {
@@ -57,8 +57,12 @@ def _oracle_row(job):
 
 
 def oracle_traces(w: Workload, layer: int, rows: list, workers: int | None = None,
-                  row_block: int | None = None, kv: str = "bf16") -> list:
-    jobs = [(w, layer, b, j, row_block, kv == "fp8") for (b, j) in rows]
+                  row_block: int | None = None, kv: str = "bf16", lens: list | None = None) -> list:
+    """Oracle traces of the given rows; ``lens`` gives batch entry b a prompt of
+    lens[b] tokens (default: the workload's prompt length), followed by the
+    workload's decode steps."""
+    jobs = [(w, layer, b, j, row_block, kv == "fp8", w.prompt if lens is None else int(lens[b]))
+            for (b, j) in rows]
     if workers is None:
         workers = min(len(jobs), max(1, (os.cpu_count() or 2) - 1))
     if workers <= 1 or len(jobs) <= 1:
@@ -155,22 +159,39 @@ def _check_codes(rep, view, scales, gpu_row, row_bits, max_slots=64):
             rep.code_mismatches.append((gpu_row, int(slot), p_))
 
 
+def _pad_garbage(x: torch.Tensor, lens: list, seed: int) -> torch.Tensor:
+    """Fills token t >= lens[b] of every batch entry b of a [B, H, T, d] bf16
+    prompt tensor with large finite values, so that any padding reaching a
+    result shows."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    noise = (torch.randn(x.shape, generator=g) * 64).to(torch.bfloat16).to(x.device)
+    t = torch.arange(x.shape[2], device=x.device)
+    pad = t[None, :] >= torch.as_tensor(lens, device=x.device)[:, None]  # [B, T]
+    return torch.where(pad[:, None, :, None], noise, x)
+
+
 def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool = False,
                set_check_every: int = 1, workers: int | None = None,
                row_block: int | None = None, traces: list | None = None,
-               kv: str = "bf16") -> Report:
+               kv: str = "bf16", lens: list | None = None) -> Report:
     """Runs one layer of workload ``w`` on the GPU and compares with the oracle.
 
     ``rows``: (b, head) pairs checked against the oracle (default: all).
     ``kv``: cache storage, "bf16" or "fp8" (the oracle then runs its FP8 mode
-    and the stored codes and scales are compared bit for bit)."""
+    and the stored codes and scales are compared bit for bit).
+    ``lens``: ragged batch (h2o_prefill_ragged): batch entry b has a prompt of
+    lens[b] <= w.prompt tokens, right-padded with garbage to w.prompt, and its
+    decode steps take its next tokens."""
     import h2o_heavy_hitter_gb300 as h2o
 
     B, H, d, T, S, k = w.batch, w.heads, w.head_dim, w.prompt, w.steps, w.k
+    if lens is not None:
+        assert not tile and len(lens) == B and all(0 <= x <= T for x in lens)
+    Tb = [T] * B if lens is None else [int(x) for x in lens]
     if rows is None:
         rows = [(b, j) for b in range(B) for j in range(H)]
     if traces is None:
-        traces = oracle_traces(w, layer, rows, workers, row_block, kv)
+        traces = oracle_traces(w, layer, rows, workers, row_block, kv, lens)
     dev = torch.device("cuda")
     N = w.tokens
 
@@ -205,8 +226,13 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
     fp8 = kv == "fp8"
     ctx = h2o.h2o_create(1, B, H, d, w.h, w.r, kv=kv)
     try:
-        out = h2o.h2o_prefill(ctx, 0, Qd[:, :, :T].contiguous(), Kd[:, :, :T].contiguous(),
-                              Vd[:, :, :T].contiguous())
+        if lens is None:
+            out = h2o.h2o_prefill(ctx, 0, Qd[:, :, :T].contiguous(), Kd[:, :, :T].contiguous(),
+                                  Vd[:, :, :T].contiguous())
+        else:
+            pq, pk, pv = (_pad_garbage(x[:, :, :T], Tb, 17 + i) for i, x in enumerate((Qd, Kd, Vd)))
+            out = h2o.h2o_prefill(ctx, 0, pq, pk, pv,
+                                  lens=torch.tensor(Tb, dtype=torch.int32, device=dev))
         view = h2o.h2o_cache_view(ctx, 0)
         scales = h2o.h2o_cache_scales(ctx, 0) if fp8 else None
         gpu_rows = torch.tensor([g for g, _ in check], device=dev)
@@ -214,8 +240,10 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
             for g, ti in check[:8]:
                 _check_codes(rep, view, scales, g, row_bits[ti])
         O = out.reshape(B * H, T, d)[gpu_rows].cpu().numpy().astype(np.float64)
-        errs = [np.abs(O[i] - traces[ti]["O"].astype(np.float64)) for i, (_, ti) in enumerate(check)]
-        if T:
+        errs = [np.abs(O[i][:Tb[g // H]] - traces[ti]["O"].astype(np.float64))
+                for i, (g, ti) in enumerate(check)]
+        errs = [e for e in errs if e.size]
+        if errs:
             rep.prefill_max_abs = float(max(e.max() for e in errs))
             rep.prefill_mean_abs = float(np.mean([e.mean() for e in errs]))
 
@@ -230,8 +258,8 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
                     rep.near_tie_mismatches += 1
                     rep.resyncs += 1
                     _, kb, vb = row_bits[ti]
-                    _resync_row(view, copies_of(g, ti), tr["kept"], tr["kept_scores"], kb, vb, k, T,
-                                scales)
+                    _resync_row(view, copies_of(g, ti), tr["kept"], tr["kept_scores"], kb, vb, k,
+                                Tb[g // H], scales)
                 else:
                     rep.mismatches.append((-1, g, gp.tolist(), tr["kept"].tolist(), tr["margin"]))
             else:
@@ -245,9 +273,10 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
                 rep.near_ties += 1
 
         dmax, dsum, dcnt = 0.0, 0.0, 0
-        qs = Qd[:, :, T:].permute(2, 0, 1, 3).contiguous()  # [S, B, H, d]
-        ks = Kd[:, :, T:].permute(2, 0, 1, 3).contiguous()
-        vs = Vd[:, :, T:].permute(2, 0, 1, 3).contiguous()
+        # decode step s of batch entry b takes its token Tb[b] + s: [S, B, H, d]
+        tok = (torch.as_tensor(Tb, device=dev)[None, :] + torch.arange(S, device=dev)[:, None])
+        bidx = torch.arange(B, device=dev)[None, :].expand(S, B)
+        qs, ks, vs = (x.permute(0, 2, 1, 3)[bidx, tok].contiguous() for x in (Qd, Kd, Vd))
         dout = torch.empty((B, H, d), dtype=torch.float32, device=dev)
         for s in range(S):
             h2o.h2o_decode_step(ctx, 0, qs[s], ks[s], vs[s], dout)
@@ -277,7 +306,7 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
                         rep.resyncs += 1
                         _, kb, vb = row_bits[ti]
                         _resync_row(view, copies_of(g, ti), tr["kept_after"][s], tr["scores_after"][s],
-                                    kb, vb, k, T + s + 1, scales)
+                                    kb, vb, k, Tb[g // H] + s + 1, scales)
                         continue
                     rep.mismatches.append((s, g, int(ev[g]), int(tr["evicted"][s]), margin))
                     continue
