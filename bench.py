@@ -163,19 +163,24 @@ def _peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def _profiled_traffic(kernel_file: str, workload: str):
+DECODE_SOURCES = ("decode.cu", "decode_kernel.cuh")  # the per-step decode kernel's source
+
+
+def _profiled_traffic(kernel_files, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the
-    current source of the kernel (its sha256 is recorded in the summary)."""
+    current source of the kernel (the sha256 of its files, concatenated in
+    order, is recorded in the summary)."""
     path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}.md")
     try:
         txt = open(path).read()
     except OSError:
         return None
-    m = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    m = re.search(r"source_sha256[^:\n]*:\s*([0-9a-f]{64})", txt)
     b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     if not (m and b):
         return None
-    src = open(os.path.join(ROOT, "h2o_heavy_hitter_gb300", "csrc", kernel_file), "rb").read()
+    src = b"".join(open(os.path.join(ROOT, "h2o_heavy_hitter_gb300", "csrc", f), "rb").read()
+                   for f in kernel_files)
     if hashlib.sha256(src).hexdigest() != m.group(1):
         return None
     return float(b.group(1))
@@ -503,6 +508,31 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     cold_ms = float(np.mean([a.elapsed_time(b_) for a, b_ in cold[1:]]))
     del flush
+
+    # ---- the same decode steps with every step of a layer in one launch
+    # (h2o_decode_steps: one CTA per row loops over the steps). Not the
+    # headline: it needs all steps' inputs in advance (a teacher-forced pass),
+    # while the timed step above launches once per step, as generation does.
+    multi_ms = None
+    if w.k <= 8192:
+        with torch.cuda.stream(stream):
+            prefill_all(ctx, L)
+            g_m = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_m, stream=stream):
+                for layer in range(L):
+                    x = ds[layer % nl]
+                    h2o.h2o_decode_steps(ctx, layer, x[0], x[1], x[2], dec_out)
+            mt = []
+            for _ in range(max(3, min(args.steps, 20))):
+                prefill_all(ctx, L)
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g_m.replay()
+                b_.record(stream)
+                mt.append((a, b_))
+        torch.cuda.synchronize()
+        multi_ms = float(np.mean([a.elapsed_time(b_) for a, b_ in mt[1:]]))
+        del g_m
     h2o.h2o_sync_check(ctx)
     ctx.close()
 
@@ -524,7 +554,7 @@ def run_ours(args, w):
     value = tokens / (elapsed_ms * 1e-3)
     roof = {"kernel": "h2o decode_kernel", "bound": "hbm", "achieved": achieved,
             "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-            "traffic": _profiled_traffic("decode.cu", w.name) if args.kv == "bf16" else None,
+            "traffic": _profiled_traffic(DECODE_SOURCES, w.name) if args.kv == "bf16" else None,
             "bytes_per_launch": bytes_per_launch,
             "launch_ms": dec_launch_ms,
             "peak_source": f"{peak_kind} hbm_gbs"}
@@ -551,6 +581,15 @@ def run_ours(args, w):
         "gpu_launches": (PREFILL_LAUNCHES + S) * L * args.steps,
         "clocks": clk,
     }
+    if multi_ms is not None:
+        a_m = bytes_per_launch * S * L / (multi_ms * 1e-3) / 1e9
+        line["decode_multistep"] = {
+            "call": "h2o_decode_steps, one launch per layer for all its decode steps",
+            "decode_ms": multi_ms, "us_per_layer_step": 1e3 * multi_ms / (S * L),
+            "decode_only_tokens_per_s": B * S / (multi_ms * 1e-3),
+            "step_tokens_per_s": B * S / ((multi_ms + prefill_ms) * 1e-3),
+            "achieved": a_m, "frac": a_m / hbm, "unit": "GB/s",
+            "note": "same algorithmic bytes per row-step as the per-step kernel"}
     if timer is not None:
         v, wall = timer.run_once()
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": timer.cores, "kind": "oracle",

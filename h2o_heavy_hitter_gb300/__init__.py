@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "H2OError", "H2OContext", "load_library", "h2o_create", "h2o_destroy", "h2o_prefill",
-    "h2o_decode_step", "h2o_prefill_attention", "h2o_cache_positions", "h2o_last_evicted",
+    "h2o_decode_step", "h2o_decode_steps", "h2o_prefill_attention", "h2o_cache_positions", "h2o_last_evicted",
     "h2o_cache_view", "h2o_cache_scales", "h2o_sync_check", "LIB_PATH", "KV_FORMATS",
 ]
 
@@ -57,6 +57,7 @@ def load_library() -> ctypes.CDLL:
         "h2o_prefill": (I, [P, I, P, P, P, I, P]),
         "h2o_prefill_ragged": (I, [P, I, P, P, P, I, P, P]),
         "h2o_decode_step": (I, [P, I, P, P, P, P]),
+        "h2o_decode_steps": (I, [P, I, I, P, P, P, P, P]),
         "h2o_prefill_attention": (I, [P, P, P, I, I, I, P, P]),
         "h2o_cache_positions": (I, [P, I, I32P]),
         "h2o_last_evicted": (I, [P, I, I32P]),
@@ -185,6 +186,25 @@ def h2o_decode_step(ctx: H2OContext, layer: int, q, k_new, v_new, out=None) -> t
     pv = _dev_ptr(v_new, torch.bfloat16, shape, "v_new")
     po = _dev_ptr(out, torch.float32, shape, "out")
     _check(load_library().h2o_decode_step(ctypes.c_void_p(ctx.handle), layer, pq, pk, pv, po))
+    return out
+
+
+def h2o_decode_steps(ctx: H2OContext, layer: int, q, k_new, v_new, out=None,
+                     evicted=None) -> torch.Tensor:
+    """``S`` decode steps of one layer from inputs [S, B, H, d] known in advance;
+    returns the fp32 outputs [S, B, H, d]. ``evicted``: optional CUDA int32
+    tensor [S, B * H] receiving each step's evicted position per row."""
+    S = q.shape[0]
+    shape = (S, ctx.batch, ctx.heads, ctx.head_dim)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.float32, device=q.device)
+    pq = _dev_ptr(q, torch.bfloat16, shape, "q")
+    pk = _dev_ptr(k_new, torch.bfloat16, shape, "k_new")
+    pv = _dev_ptr(v_new, torch.bfloat16, shape, "v_new")
+    po = _dev_ptr(out, torch.float32, shape, "out")
+    pe = 0 if evicted is None else _dev_ptr(evicted, torch.int32, (S, ctx.rows), "evicted")
+    _check(load_library().h2o_decode_steps(ctypes.c_void_p(ctx.handle), layer, S, pq, pk, pv, po,
+                                           pe or None))
     return out
 
 

@@ -74,7 +74,8 @@ struct h2o_ctx {
   int32_t* counter = nullptr; // decode scratch, per layer [rows], zero between steps
   int32_t* err = nullptr;     // device error word
   std::vector<int> prompt_len;  // per layer: -1 until prefilled
-  h2o::DecodeConfig dcfg{};
+  h2o::DecodeConfig dcfg{};   // one step per launch
+  h2o::DecodeConfig mcfg{};   // several steps per launch (h2o_decode_steps)
 
   void* layer_K(int l) const { return K + static_cast<size_t>(l) * kv_elems_per_layer * kv_elem_bytes; }
   void* layer_V(int l) const { return V + static_cast<size_t>(l) * kv_elems_per_layer * kv_elem_bytes; }
@@ -212,6 +213,7 @@ int h2o_create_ex(int layers, int batch, int heads, int head_dim, int h, int r, 
                          env_int("H2O_DECODE_SEGS"), env_int("H2O_DECODE_PDL"),
                          env_int("H2O_DECODE_PIPE")};
   c->dcfg = h2o::decode_config(c->rows, c->k, c->d, sms, tune, kv_format == H2O_KV_FP8);
+  c->mcfg = h2o::decode_multi_config(c->rows, c->k, c->d, sms, kv_format == H2O_KV_FP8);
 
   const size_t L = layers, R = c->rows, K = c->k, D = head_dim;
   c->kv_elems_per_layer = R * K * D;
@@ -327,11 +329,11 @@ int h2o_prefill_attention_noalloc(const void* Q, const void* K, const void* V, i
   return H2O_OK;
 }
 
-int h2o_decode_step(h2o_ctx* c, int layer, const void* q, const void* k_new, const void* v_new,
-                    float* out) {
-  if (int rc = check_layer(c, layer)) return rc;
-  if (!q || !k_new || !v_new || !out) return fail(H2O_EINVAL, "null q, k_new, v_new or out");
-  if (c->prompt_len[layer] < 0) return fail(H2O_ESTATE, "decode step before prefill of this layer");
+}  // extern "C"
+
+namespace {
+
+h2o::DecodeArgs decode_args(h2o_ctx* c, int layer) {
   h2o::DecodeArgs a{};
   a.Kc = c->layer_K(layer);
   a.Vc = c->layer_V(layer);
@@ -343,17 +345,69 @@ int h2o_decode_step(h2o_ctx* c, int layer, const void* q, const void* k_new, con
   a.logits = c->layer_logits(layer);
   a.partial = c->layer_partial(layer);
   a.counter = c->layer_counter(layer);
-  a.q = q;
-  a.k_new = k_new;
-  a.v_new = v_new;
-  a.out = out;
+  a.rows = c->rows;
+  a.steps = 1;
   a.k = c->k;
   a.r = c->r;
   a.segs = c->dcfg.segs;
   a.seg_len = c->dcfg.seg_len;
   a.qscale = h2o::kLog2e / std::sqrt(static_cast<float>(c->d));
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int h2o_decode_step(h2o_ctx* c, int layer, const void* q, const void* k_new, const void* v_new,
+                    float* out) {
+  if (int rc = check_layer(c, layer)) return rc;
+  if (!q || !k_new || !v_new || !out) return fail(H2O_EINVAL, "null q, k_new, v_new or out");
+  if (c->prompt_len[layer] < 0) return fail(H2O_ESTATE, "decode step before prefill of this layer");
+  h2o::DecodeArgs a = decode_args(c, layer);
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.out = out;
   cudaError_t e = h2o::decode_launch(a, c->dcfg, c->rows, c->d, current_stream());
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return H2O_OK;
+}
+
+int h2o_decode_steps(h2o_ctx* c, int layer, int steps, const void* q, const void* k_new,
+                     const void* v_new, float* out, int32_t* evicted) {
+  if (int rc = check_layer(c, layer)) return rc;
+  if (steps < 0) return fail(H2O_EINVAL, "steps must be >= 0");
+  if (steps == 0) return H2O_OK;
+  if (!q || !k_new || !v_new || !out) return fail(H2O_EINVAL, "null q, k_new, v_new or out");
+  if (c->prompt_len[layer] < 0) return fail(H2O_ESTATE, "decode step before prefill of this layer");
+  h2o::DecodeArgs a = decode_args(c, layer);
+  cudaStream_t s = current_stream();
+  cudaError_t e;
+  if (c->k <= h2o::kMultiMaxSlots) {
+    a.q = q;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.out = out;
+    a.evicted = evicted;
+    a.steps = steps;
+    a.segs = 1;
+    a.seg_len = c->k;
+    e = h2o::decode_multi_launch(a, c->mcfg, c->rows, c->d, s);
+    if (e != cudaSuccess) return cuda_fail(e, "multi-step decode launch");
+    return H2O_OK;
+  }
+  // budgets too large for one CTA per row: one launch per step
+  const size_t in_step = static_cast<size_t>(c->rows) * c->d;
+  for (int i = 0; i < steps; ++i) {
+    a.q = static_cast<const uint16_t*>(q) + i * in_step;
+    a.k_new = static_cast<const uint16_t*>(k_new) + i * in_step;
+    a.v_new = static_cast<const uint16_t*>(v_new) + i * in_step;
+    a.out = out + i * in_step;
+    a.evicted = evicted ? evicted + static_cast<size_t>(i) * c->rows : nullptr;
+    e = h2o::decode_launch(a, c->dcfg, c->rows, c->d, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  }
   return H2O_OK;
 }
 

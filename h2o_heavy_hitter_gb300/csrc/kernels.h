@@ -24,10 +24,13 @@ struct DecodeArgs {
   float* logits;      // [rows][k] scratch: this step's base-2 logits
   float* partial;     // [rows][segs][d + 4] scratch: {max, sum, -, -, output[d]} per segment
   int32_t* counter;   // [rows] scratch: segments arrived this step (0 between steps)
-  const void* q;      // bf16 [rows][d]
-  const void* k_new;  // bf16 [rows][d]
-  const void* v_new;  // bf16 [rows][d]
-  float* out;         // [rows][d]
+  const void* q;      // bf16 [steps][rows][d]
+  const void* k_new;  // bf16 [steps][rows][d]
+  const void* v_new;  // bf16 [steps][rows][d]
+  float* out;         // [steps][rows][d]
+  int32_t* evicted;   // [steps][rows] evicted position (-1 none) of each step, or null
+  int rows;           // rows of the layer
+  int steps;          // steps per launch (1 except for the multi-step launcher)
   int k;              // slots per row (h + r)
   int r;              // recent window
   int segs;           // CTAs per row
@@ -58,6 +61,15 @@ DecodeConfig decode_config(int rows, int k, int d, int num_sms, const DecodeTuni
                            bool fp8);
 cudaError_t decode_launch(const DecodeArgs& a, const DecodeConfig& cfg, int rows, int d,
                           cudaStream_t stream);
+
+// Several steps in one launch: one CTA per row runs a.steps consecutive steps
+// (needs k <= kMultiMaxSlots, whose logits stay in shared memory). The launch
+// shape follows decode_config with one segment per row: 128 threads for many
+// rows, else 256 with two batches in flight.
+constexpr int kMultiMaxSlots = 8192;
+DecodeConfig decode_multi_config(int rows, int k, int d, int num_sms, bool fp8);
+cudaError_t decode_multi_launch(const DecodeArgs& a, const DecodeConfig& cfg, int rows, int d,
+                                cudaStream_t stream);
 
 // ---- prefill -----------------------------------------------------------------
 // Row stride (floats) of the per-row log-sum-exp scratch: T rounded up to a

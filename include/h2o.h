@@ -175,6 +175,25 @@ int h2o_decode_step(h2o_ctx* ctx, int layer, const void* q, const void* k_new, c
                     float* out);
 
 /*
+ * h2o_decode_steps - `steps` consecutive h2o_decode_step calls of one layer
+ * whose inputs are all known in advance ([H2O] 4.1: the policy is the same
+ * greedy step repeated; 5, Ablation and Extended Evaluations: streaming over
+ * long inputs), e.g. a teacher-forced pass over a known continuation, one
+ * layer after the other. Results equal those of the single steps.
+ *
+ * q, k_new, v_new: device bf16 [steps, batch, heads, d]; out: device fp32
+ * [steps, batch, heads, d]; evicted: device int32 [steps, batch * heads], the
+ * position evicted by each row at each step (-1: none, the new token's own
+ * position when it is dropped), or NULL. With h + r <= 8192 all steps run in
+ * one launch, one CTA per row looping over its steps (no per-step launch and
+ * drain); larger budgets take one launch per step. steps >= 0 (0: nothing is
+ * done). Allocates nothing and never synchronises; capturable in a CUDA
+ * graph. Errors: H2O_EINVAL, H2O_ESTATE (layer never prefilled), H2O_ECUDA.
+ */
+int h2o_decode_steps(h2o_ctx* ctx, int layer, int steps, const void* q, const void* k_new,
+                     const void* v_new, float* out, int32_t* evicted);
+
+/*
  * h2o_prefill_attention - the attention part of prefill, without touching any
  * cache: causal attention of `rows` independent rows of T tokens, the output
  * and every token's column-sum score.

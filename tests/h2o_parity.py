@@ -170,10 +170,66 @@ def _pad_garbage(x: torch.Tensor, lens: list, seed: int) -> torch.Tensor:
     return torch.where(pad[:, None, :, None], noise, x)
 
 
+def _check_multi(rep, h2o, ctx, view, check, traces, qs, ks, vs, copies, set_check_every):
+    """Runs every decode step in one h2o_decode_steps call and compares each
+    step's outputs and evictions, then the final retained sets, with the oracle."""
+    S, B, H, d = qs.shape
+    out = torch.empty((S, B, H, d), dtype=torch.float32, device=qs.device)
+    ev = torch.full((S, B * H), -7, dtype=torch.int32, device=qs.device)
+    h2o.h2o_decode_steps(ctx, 0, qs, ks, vs, out, ev)
+    o = out.reshape(S, B * H, d).cpu().numpy().astype(np.float64)
+    ev = ev.cpu().numpy()
+    dmax, dsum, dcnt = 0.0, 0.0, 0
+    diverged = set()
+    for s in range(S):
+        if copies is not None:
+            for i in range(int(copies.max()) + 1):
+                same = ev[s][copies == i]
+                if not np.all(same == same[0]):
+                    rep.mismatches.append((s, "copies", i, same.tolist(), None))
+        for g, ti in check:
+            if ti in diverged:
+                continue
+            tr = traces[ti]
+            e = np.abs(o[s, g] - tr["outs"][s])
+            dmax = max(dmax, float(e.max()))
+            dsum += float(e.sum())
+            dcnt += e.size
+            rep.evict_checks += 1
+            near = tr["margins"][s] < oracle.NEAR_TIE
+            rep.near_ties += int(near)
+            if ev[s, g] != tr["evicted"][s]:
+                if near:
+                    rep.near_tie_mismatches += 1
+                    diverged.add(ti)
+                else:
+                    rep.mismatches.append((s, g, int(ev[s, g]), int(tr["evicted"][s]),
+                                           tr["margins"][s]))
+    if set_check_every:
+        pos = h2o.h2o_cache_positions(ctx, 0)
+        scores = view["score"].cpu().numpy()
+        for g, ti in check:
+            if ti in diverged:
+                continue
+            tr = traces[ti]
+            gp = np.sort(pos[g][pos[g] >= 0])
+            rep.set_checks += 1
+            if not np.array_equal(gp, tr["kept_after"][-1]):
+                rep.mismatches.append((S - 1, g, "set", gp.tolist(), tr["kept_after"][-1].tolist()))
+            else:
+                by_pos = dict(zip(pos[g].tolist(), scores[g].tolist()))
+                ref = tr["scores_after"][-1]
+                got = np.array([by_pos[p] for p in tr["kept_after"][-1].tolist()])
+                if len(ref):
+                    rel = np.max(np.abs(got - ref) / np.maximum(ref, 1e-30))
+                    rep.score_max_rel = max(rep.score_max_rel, float(rel))
+    return dmax, dsum, dcnt
+
+
 def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool = False,
                set_check_every: int = 1, workers: int | None = None,
                row_block: int | None = None, traces: list | None = None,
-               kv: str = "bf16", lens: list | None = None) -> Report:
+               kv: str = "bf16", lens: list | None = None, decode: str = "step") -> Report:
     """Runs one layer of workload ``w`` on the GPU and compares with the oracle.
 
     ``rows``: (b, head) pairs checked against the oracle (default: all).
@@ -181,7 +237,12 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
     and the stored codes and scales are compared bit for bit).
     ``lens``: ragged batch (h2o_prefill_ragged): batch entry b has a prompt of
     lens[b] <= w.prompt tokens, right-padded with garbage to w.prompt, and its
-    decode steps take its next tokens."""
+    decode steps take its next tokens.
+    ``decode``: "step" (one h2o_decode_step per step, checked and resynchronised
+    after each) or "multi" (all steps in one h2o_decode_steps call, checked
+    afterwards from the per-step outputs and evicted positions; a row whose
+    eviction differs from the oracle's at a near-tie is counted and no longer
+    compared, since nothing can be resynchronised inside the call)."""
     import h2o_heavy_hitter_gb300 as h2o
 
     B, H, d, T, S, k = w.batch, w.heads, w.head_dim, w.prompt, w.steps, w.k
@@ -278,7 +339,13 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
         bidx = torch.arange(B, device=dev)[None, :].expand(S, B)
         qs, ks, vs = (x.permute(0, 2, 1, 3)[bidx, tok].contiguous() for x in (Qd, Kd, Vd))
         dout = torch.empty((B, H, d), dtype=torch.float32, device=dev)
-        for s in range(S):
+        if decode == "multi":
+            dmax, dsum, dcnt = _check_multi(rep, h2o, ctx, view, check, traces, qs, ks, vs, copies,
+                                            set_check_every)
+            S_loop = 0
+        else:
+            S_loop = S
+        for s in range(S_loop):
             h2o.h2o_decode_step(ctx, 0, qs[s], ks[s], vs[s], dout)
             ev = h2o.h2o_last_evicted(ctx, 0)
             o = dout.reshape(B * H, d)[gpu_rows].cpu().numpy().astype(np.float64)
