@@ -131,6 +131,30 @@ def row_tokens(w: Workload, layer: int, b: int, head: int, u: np.ndarray | None 
     return bits[0], bits[1], bits[2]
 
 
+def stream_chunk(seed: int, chunk: int, steps: int, rows: int, d: int):
+    """bf16 bits (uint16) of q, k, v for chunk `chunk` of a long decode stream:
+    three arrays [steps, rows, d], the inputs of decode steps
+    chunk * steps .. (chunk + 1) * steps - 1 of every row.
+
+    For streams too long to draw at once (millions of steps): each chunk has its
+    own Generator, SeedSequence([1, seed, chunk]), so any chunk can be drawn
+    alone. Same construction as row_tokens with one unit direction u per stream
+    (SeedSequence([1, seed, U_STREAM])), except that a key's power-law amplitude
+    uses a rank drawn uniformly from 1 .. 2^20 instead of a permutation of the
+    row's tokens: a_t = 4 * rank_t ** -0.8."""
+    ru = np.random.default_rng(np.random.SeedSequence([1, seed, U_STREAM]))
+    u = ru.standard_normal(d, dtype=np.float32)
+    u = (u / np.float32(np.linalg.norm(u.astype(np.float64)))).astype(np.float32)
+    rng = np.random.default_rng(np.random.SeedSequence([1, seed, chunk]))
+    x = rng.standard_normal((3, steps, rows, d), dtype=np.float32)
+    rank = rng.integers(1, 1 << 20, size=(steps, rows), endpoint=True).astype(np.float32)
+    a = (np.float32(4.0) * np.power(rank, np.float32(-0.8))).astype(np.float32)
+    x[1] += a[..., None] * u
+    x[0] += np.float32(2.0) * u
+    bits = f32_to_bf16_bits(x)
+    return bits[0], bits[1], bits[2]
+
+
 def layer_tokens(w: Workload, layer: int, rows: list[tuple[int, int]] | None = None):
     """bf16 bits of q, k, v for one layer: arrays [B, H, N, d] (uint16).
 
