@@ -340,7 +340,7 @@ def run_ours(args, w):
     pre_out = torch.empty((B, H, T, d), dtype=torch.float32, device=dev)
     dec_out = torch.empty((S, B, H, d), dtype=torch.float32, device=dev)
 
-    ctx = h2o.h2o_create(L, B, H, d, w.h, w.r, kv=args.kv)
+    ctx = h2o.h2o_create(L, B, H, d, w.h, w.r, kv=args.kv, layout=args.layout)
     stream = torch.cuda.Stream(device=dev)
 
     def prefill_all(c, layers, prompt=None):
@@ -470,7 +470,7 @@ def run_ours(args, w):
     need = -(-2 * l2_bytes // _layer_cache_bytes(w, args.kv))
     if _layer_cache_bytes(w, args.kv) * L <= l2_bytes and need <= MAX_CYCLED_LAYERS:
         n_cycle = max(2, need)
-        ctx_c = h2o.h2o_create(n_cycle, B, H, d, w.h, w.r, kv=args.kv)
+        ctx_c = h2o.h2o_create(n_cycle, B, H, d, w.h, w.r, kv=args.kv, layout=args.layout)
         sc = min(S, 32)
         with torch.cuda.stream(stream):
             prefill_all(ctx_c, n_cycle)
@@ -514,7 +514,7 @@ def run_ours(args, w):
     # headline: it needs all steps' inputs in advance (a teacher-forced pass),
     # while the timed step above launches once per step, as generation does.
     multi_ms = None
-    if w.k <= 8192:
+    if w.k <= 8192 and args.layout == "slots":
         with torch.cuda.stream(stream):
             prefill_all(ctx, L)
             g_m = torch.cuda.CUDAGraph()
@@ -543,7 +543,7 @@ def run_ours(args, w):
 
     peaks, peak_kind = _peaks()
     rows = B * H
-    bytes_per_launch = decode_bytes_per_row_step(w.k, d, args.kv) * rows
+    bytes_per_launch = decode_bytes_per_row_step(w.k, d, args.kv, args.layout, w.h) * rows
     dec_launch_ms = decode_ms / (S * L)  # graph replay: launch gaps included
     achieved = bytes_per_launch / (dec_launch_ms * 1e-3) / 1e9
     achieved_cold = bytes_per_launch / (cold_ms * 1e-3) / 1e9
@@ -554,7 +554,8 @@ def run_ours(args, w):
     value = tokens / (elapsed_ms * 1e-3)
     roof = {"kernel": "h2o decode_kernel", "bound": "hbm", "achieved": achieved,
             "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-            "traffic": _profiled_traffic(DECODE_SOURCES, w.name) if args.kv == "bf16" else None,
+            "traffic": (_profiled_traffic(DECODE_SOURCES, w.name)
+                        if args.kv == "bf16" and args.layout == "slots" else None),
             "bytes_per_launch": bytes_per_launch,
             "launch_ms": dec_launch_ms,
             "peak_source": f"{peak_kind} hbm_gbs"}
@@ -568,7 +569,7 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": _data_desc(w),
-        "config": dict(_config(w, l2_bytes), kv_cache=args.kv),
+        "config": dict(_config(w, l2_bytes), kv_cache=args.kv, cache_layout=args.layout),
         "roofline": roof,
         "phases": {"prefill_ms": prefill_ms, "decode_ms": decode_ms,
                    "prefill_tokens_per_s": B * T * L / (prefill_ms * 1e-3),
@@ -611,6 +612,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="cache storage: bf16, or E4M3 codes with per-token scales")
+    ap.add_argument("--layout", default="slots", choices=["slots", "ring"],
+                    help="cache layout: slot-indexed, or heavy slots plus a circular recent window")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

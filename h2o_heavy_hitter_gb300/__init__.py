@@ -131,21 +131,29 @@ class H2OContext:
         self.close()
 
 
+H2O_LAYOUT_RING = 0x100
+
+
 def h2o_create(layers: int, batch: int, heads: int, head_dim: int, h: int, r: int,
-               kv: str = "bf16") -> H2OContext:
+               kv: str = "bf16", layout: str = "slots") -> H2OContext:
     """Cache of `layers` layers; kv "bf16" (h2o_create) or "fp8" (E4M3 codes with
-    per-token scales, h2o_create_ex)."""
+    per-token scales, h2o_create_ex); layout "slots" (slot-indexed) or "ring"
+    (heavy slots then the recent window as a circular queue, bf16 only)."""
     _need_cuda()
     if kv not in KV_FORMATS:
         raise ValueError(f"kv must be one of {sorted(KV_FORMATS)}")
+    if layout not in ("slots", "ring"):
+        raise ValueError('layout must be "slots" or "ring"')
     lib = load_library()
     out = ctypes.c_void_p()
-    if kv == "bf16":
+    if kv == "bf16" and layout == "slots":
         _check(lib.h2o_create(layers, batch, heads, head_dim, h, r, ctypes.byref(out)))
     else:
-        _check(lib.h2o_create_ex(layers, batch, heads, head_dim, h, r, KV_FORMATS[kv],
-                                 ctypes.byref(out)))
-    return H2OContext(out.value, layers, batch, heads, head_dim, h, r, kv)
+        fmt = KV_FORMATS[kv] | (H2O_LAYOUT_RING if layout == "ring" else 0)
+        _check(lib.h2o_create_ex(layers, batch, heads, head_dim, h, r, fmt, ctypes.byref(out)))
+    ctx = H2OContext(out.value, layers, batch, heads, head_dim, h, r, kv)
+    ctx.layout = layout
+    return ctx
 
 
 def h2o_destroy(ctx: H2OContext) -> None:

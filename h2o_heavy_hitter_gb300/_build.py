@@ -22,7 +22,7 @@ INCLUDE = ROOT / "include"
 BUILD = PKG / "_build"
 LIB = PKG / "libh2o.so"
 
-CU_SOURCES = ["decode.cu", "decode_multi.cu", "prefill.cu", "select.cu"]
+CU_SOURCES = ["decode.cu", "decode_multi.cu", "decode_ring.cu", "prefill.cu", "select.cu"]
 CPP_SOURCES = ["h2o_api.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

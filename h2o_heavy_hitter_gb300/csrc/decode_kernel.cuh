@@ -145,6 +145,7 @@ struct DecodeShared {
   int wslot[NW];
   int is_last;
   int target;
+  float lv_score;  // ring layout: updated score of the token leaving the recent window
 };
 
 // PIPE: two batches of U slots per group in flight (software pipelining).
@@ -154,8 +155,15 @@ struct DecodeShared {
 // in one launch, with step s's inputs and output at offset s * rows * d; the
 // steps are separated by block barriers and the cache is read with coherent
 // loads, since a step reads the slot the previous step wrote.
-template <int D, int NT, int U, bool PIPE, bool F8, bool MULTI = false>
+// RING (bf16 cache, r >= 1): the layout of the pages' implementation -- heavy
+// slots [0, h) filled from 0, and the recent window as a circular queue, the
+// token at position p in slot h + p mod r. The recent slots' positions are
+// implied by t and never read; the eviction candidates are the heavy slots
+// and the token leaving the window (position t - r, in the slot the new token
+// takes). When a heavy slot is evicted the leaving token moves into it.
+template <int D, int NT, int U, bool PIPE, bool F8, bool MULTI = false, bool RING = false>
 __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
+  static_assert(!(RING && F8), "the ring layout is built for the bf16 cache");
   using Sm = DecodeShared<D, NT>;
   constexpr int LPS = Sm::LPS, G = Sm::G, NW = Sm::NW;
   constexpr int PS = D + 4;  // partial stride: {max, sum, -, -, output[D]}
@@ -201,6 +209,20 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   const int count = meta[0];
   const int t = meta[1];
   const int n = max(0, min(cap, count - s0));
+  // ring layout: recent slots in use, heavy slots in use, the slot of position t - r (and t)
+  const int nring = RING ? min(t, a.r) : 0;
+  const int nh = RING ? count - nring : 0;
+  const int lv = RING ? a.h + t % a.r : -1;
+  // slot gi of the row holds a token (ring layout)
+  auto occ_g = [&](int gi) -> bool { return gi < nh || (gi >= a.h && gi < a.h + nring); };
+  // slot s0 + i of this segment holds a token (a batch may reach past the
+  // segment's last slot: those lanes loaded nothing)
+  auto occ = [&](int i) -> bool {
+    if constexpr (RING)
+      return i < cap && occ_g(s0 + i);
+    else
+      return i < n;
+  };
   {  // the row's finishing CTA reads these scores and positions: warm L2 now
     const int lines = (cap * 4 + 127) / 128 + 1;
     for (int i = tid; i < 2 * lines; i += NT) {
@@ -225,14 +247,15 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   // Single-CTA rows: this thread's slots' scores and positions, loaded now so
   // that their latency hides behind the K/V sweep.
   const int filled = min(count, a.k);
+  const int slot_end = RING ? a.k : filled;  // slots the finish visits (occupied or not)
   float sc_r[kSoloRegs];
   int ps_r[kSoloRegs];
 #pragma unroll
   for (int jj = 0; jj < kSoloRegs; ++jj) {
     const int i = tid + jj * NT;
-    if (solo && i < filled) {
+    if (solo && i < slot_end && (!RING || occ_g(i))) {
       sc_r[jj] = a.score[rk + i];
-      ps_r[jj] = a.pos[rk + i];
+      ps_r[jj] = !RING || i < a.h ? a.pos[rk + i] : 0;  // recent positions are implied
     }
   }
   // One batch: U slots of this group, loaded by capacity (slots past the fill
@@ -278,7 +301,7 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
     float bm = m;
 #pragma unroll
     for (int u = 0; u < U; ++u)
-      if (base + u * G < n) bm = fmaxf(bm, s[u]);
+      if (occ(base + u * G)) bm = fmaxf(bm, s[u]);
     const float corr = ex2(m - bm);
     lsum *= corr;
 #pragma unroll
@@ -287,7 +310,7 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int i = base + u * G;
-      if (i < n) {
+      if (occ(i)) {
         const float p = ex2(s[u] - bm);
         lsum += p;
         if constexpr (F8)
@@ -457,7 +480,8 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   unsigned long long best = ~0ull;
   int bslot = -1;
 #pragma unroll 1
-  for (int jj = 0, i = tid; i < filled; ++jj, i += NT) {
+  for (int jj = 0, i = tid; i < slot_end; ++jj, i += NT) {
+    if (RING && !occ_g(i)) continue;
     float sc;
     int ps;
     if (solo && jj < kSoloRegs) {
@@ -469,11 +493,18 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
         }
     } else {
       sc = a.score[rk + i];
-      ps = a.pos[rk + i];
+      ps = !RING || i < a.h ? a.pos[rk + i] : 0;
     }
     const float lg = solo ? solo_logits[i] : __ldcg(a.logits + rk + i);
     const float ns = sc + ex2(lg - M) * invL;
     a.score[rk + i] = ns;
+    if constexpr (RING) {
+      if (i == lv) sm.lv_score = ns;  // read by thread 0 after the barrier below
+      if (i >= a.h) {
+        if (i == lv && t >= a.r) ps = thr;  // the leaving token competes, position t - r
+        else continue;                      // the rest of the window never does
+      }
+    }
     if (ps <= thr) {
       const unsigned long long key = pack_key(ns, ps);
       if (key < best) {
@@ -513,7 +544,16 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
       }
     const bool full = count >= a.k;
     int target, evict_pos = -1;
-    if (full) {
+    if constexpr (RING) {
+      // target: the heavy slot the leaving token moves into, or -1; the new
+      // token always takes ring slot lv
+      if (full) {
+        evict_pos = static_cast<int>(b & 0xffffffffu);
+        target = bs == lv ? -1 : bs;
+      } else {
+        target = t >= a.r ? nh : -1;  // not full: the leaving token joins the heavy slots
+      }
+    } else if (full) {
       evict_pos = b == ~0ull ? -1 : static_cast<int>(b & 0xffffffffu);
       target = bs == kNewSlot ? -1 : bs;  // a dropped new token leaves the cache unchanged
     } else {
@@ -525,7 +565,14 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
     mw[1] = t + 1;
     mw[2] = evict_pos;
     if (a.evicted) a.evicted[static_cast<size_t>(step) * a.rows + row] = evict_pos;
-    if (target >= 0) {
+    if constexpr (RING) {
+      if (target >= 0) {
+        a.pos[rk + target] = t - a.r;
+        a.score[rk + target] = sm.lv_score;
+      }
+      a.pos[rk + lv] = t;  // written for readback; the kernel never reads it
+      a.score[rk + lv] = p_new;
+    } else if (target >= 0) {
       a.pos[rk + target] = t;
       a.score[rk + target] = p_new;  // after the score loop's write of this slot (barrier above)
     }
@@ -533,7 +580,22 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   }
   __syncthreads();
   const int target = sm.target;
-  if (target >= 0 && g == 0) {
+  if constexpr (RING) {
+    if (g == 0) {
+      __nv_bfloat16* Kc = static_cast<__nv_bfloat16*>(a.Kc);
+      __nv_bfloat16* Vc = static_cast<__nv_bfloat16*>(a.Vc);
+      const size_t src = (rk + lv) * D + l * 8;
+      if (target >= 0) {  // the leaving token moves into the freed heavy slot first
+        const uint4 kl = *reinterpret_cast<const uint4*>(Kc + src);
+        const uint4 vl = *reinterpret_cast<const uint4*>(Vc + src);
+        const size_t dst = (rk + target) * D + l * 8;
+        *reinterpret_cast<uint4*>(Kc + dst) = kl;
+        *reinterpret_cast<uint4*>(Vc + dst) = vl;
+      }
+      *reinterpret_cast<uint4*>(Kc + src) = knew;
+      *reinterpret_cast<uint4*>(Vc + src) = vnew;
+    }
+  } else if (target >= 0 && g == 0) {
     const size_t dst = (rk + target) * D + l * 8;
     if constexpr (F8) {
       *reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.Kc) + dst) = kcode;

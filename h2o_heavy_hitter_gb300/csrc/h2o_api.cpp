@@ -59,6 +59,7 @@ struct h2o_ctx {
   int layers, batch, heads, d, h, r, k, rows;
   int device;
   int kv_format;              // H2O_KV_BF16 or H2O_KV_FP8
+  bool ring = false;          // H2O_LAYOUT_RING: heavy slots, then the window as a circular queue
   size_t kv_elems_per_layer;  // rows * k * d
   size_t kv_elem_bytes;       // 2 (bf16) or 1 (E4M3 code)
   void* base = nullptr;       // single cache allocation
@@ -144,8 +145,8 @@ int prefill_layer(h2o_ctx* c, int layer, const void* Q, const void* K, const voi
                            static_cast<float*>(colsum.p), c->err, s);
     if (rc) return rc;
     e = h2o::prefill_select(static_cast<float*>(colsum.p), c->rows, T, lens, heads, c->h, c->r,
-                            c->layer_score(layer), c->layer_pos(layer), c->layer_meta(layer),
-                            c->err, s);
+                            c->ring, c->layer_score(layer), c->layer_pos(layer),
+                            c->layer_meta(layer), c->err, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill select launch");
     e = c->kv_format == H2O_KV_FP8
             ? h2o::prefill_gather_fp8(K, V, c->rows, T, c->d, c->k, c->layer_pos(layer),
@@ -175,8 +176,12 @@ int h2o_create_ex(int layers, int batch, int heads, int head_dim, int h, int r, 
                   h2o_ctx** out) {
   if (!out) return fail(H2O_EINVAL, "null output pointer");
   *out = nullptr;
+  const bool ring = (kv_format & H2O_LAYOUT_RING) != 0;
+  kv_format &= ~H2O_LAYOUT_RING;
   if (kv_format != H2O_KV_BF16 && kv_format != H2O_KV_FP8)
-    return fail(H2O_EINVAL, "kv_format must be H2O_KV_BF16 or H2O_KV_FP8");
+    return fail(H2O_EINVAL, "kv_format must be H2O_KV_BF16 or H2O_KV_FP8, optionally | H2O_LAYOUT_RING");
+  if (ring && (kv_format != H2O_KV_BF16 || r < 1))
+    return fail(H2O_EINVAL, "H2O_LAYOUT_RING needs the bf16 cache and r >= 1");
   if (layers < 1 || batch < 1 || heads < 1) return fail(H2O_EINVAL, "layers, batch and heads must be >= 1");
   if (head_dim != 64 && head_dim != 128) return fail(H2O_EINVAL, "head_dim must be 64 or 128");
   if (h < 0 || r < 0 || h + r < 1 || h + r > H2O_MAX_K)
@@ -194,6 +199,7 @@ int h2o_create_ex(int layers, int batch, int heads, int head_dim, int h, int r, 
   c->k = h + r;
   c->rows = static_cast<int>(rows_l);
   c->kv_format = kv_format;
+  c->ring = ring;
   c->kv_elem_bytes = kv_format == H2O_KV_FP8 ? 1 : 2;
   c->prompt_len.assign(layers, -1);
   try {
@@ -348,6 +354,7 @@ h2o::DecodeArgs decode_args(h2o_ctx* c, int layer) {
   a.rows = c->rows;
   a.steps = 1;
   a.k = c->k;
+  a.h = c->h;
   a.r = c->r;
   a.segs = c->dcfg.segs;
   a.seg_len = c->dcfg.seg_len;
@@ -369,7 +376,8 @@ int h2o_decode_step(h2o_ctx* c, int layer, const void* q, const void* k_new, con
   a.k_new = k_new;
   a.v_new = v_new;
   a.out = out;
-  cudaError_t e = h2o::decode_launch(a, c->dcfg, c->rows, c->d, current_stream());
+  cudaError_t e = c->ring ? h2o::decode_ring_launch(a, c->dcfg, c->rows, c->d, current_stream())
+                          : h2o::decode_launch(a, c->dcfg, c->rows, c->d, current_stream());
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return H2O_OK;
 }
@@ -384,7 +392,7 @@ int h2o_decode_steps(h2o_ctx* c, int layer, int steps, const void* q, const void
   h2o::DecodeArgs a = decode_args(c, layer);
   cudaStream_t s = current_stream();
   cudaError_t e;
-  if (c->k <= h2o::kMultiMaxSlots) {
+  if (c->k <= h2o::kMultiMaxSlots && !c->ring) {
     a.q = q;
     a.k_new = k_new;
     a.v_new = v_new;
@@ -397,7 +405,7 @@ int h2o_decode_steps(h2o_ctx* c, int layer, int steps, const void* q, const void
     if (e != cudaSuccess) return cuda_fail(e, "multi-step decode launch");
     return H2O_OK;
   }
-  // budgets too large for one CTA per row: one launch per step
+  // budgets too large for one CTA per row, or the ring layout: one launch per step
   const size_t in_step = static_cast<size_t>(c->rows) * c->d;
   for (int i = 0; i < steps; ++i) {
     a.q = static_cast<const uint16_t*>(q) + i * in_step;
@@ -405,7 +413,8 @@ int h2o_decode_steps(h2o_ctx* c, int layer, int steps, const void* q, const void
     a.v_new = static_cast<const uint16_t*>(v_new) + i * in_step;
     a.out = out + i * in_step;
     a.evicted = evicted ? evicted + static_cast<size_t>(i) * c->rows : nullptr;
-    e = h2o::decode_launch(a, c->dcfg, c->rows, c->d, s);
+    e = c->ring ? h2o::decode_ring_launch(a, c->dcfg, c->rows, c->d, s)
+                : h2o::decode_launch(a, c->dcfg, c->rows, c->d, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   }
   return H2O_OK;

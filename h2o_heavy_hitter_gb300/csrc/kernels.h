@@ -32,6 +32,7 @@ struct DecodeArgs {
   int rows;           // rows of the layer
   int steps;          // steps per launch (1 except for the multi-step launcher)
   int k;              // slots per row (h + r)
+  int h;              // heavy slots (ring layout: slots [0, h), the window after them)
   int r;              // recent window
   int segs;           // CTAs per row
   int seg_len;        // slots per segment (the last may be shorter)
@@ -61,6 +62,10 @@ DecodeConfig decode_config(int rows, int k, int d, int num_sms, const DecodeTuni
                            bool fp8);
 cudaError_t decode_launch(const DecodeArgs& a, const DecodeConfig& cfg, int rows, int d,
                           cudaStream_t stream);
+// The same step for a cache in the ring layout (bf16, r >= 1): heavy slots
+// [0, h), the token at recent position p in slot h + p mod r.
+cudaError_t decode_ring_launch(const DecodeArgs& a, const DecodeConfig& cfg, int rows, int d,
+                               cudaStream_t stream);
 
 // Several steps in one launch: one CTA per row runs a.steps consecutive steps
 // (needs k <= kMultiMaxSlots, whose logits stay in shared memory). The launch
@@ -97,10 +102,13 @@ cudaError_t noalloc_lse_scratch(float** out);
 
 // Top-h plus recent selection of every row into the cache's pos/score/meta
 // (colsum rows T floats apart; per-row lengths as for prefill_forward; a
-// length outside [0, T] is clamped and sets kErrBadLength in *err).
+// length outside [0, T] is clamped and sets kErrBadLength in *err). `ring`:
+// kept tokens older than the window fill slots [0, h) in ascending order and
+// a window token at position p goes to slot h + p mod r; otherwise every kept
+// token is compacted in ascending order from slot 0.
 cudaError_t prefill_select(const float* colsum, int rows, int T, const int32_t* lens, int heads,
-                           int h, int r, float* score, int32_t* pos, int32_t* meta, int32_t* err,
-                           cudaStream_t stream);
+                           int h, int r, bool ring, float* score, int32_t* pos, int32_t* meta,
+                           int32_t* err, cudaStream_t stream);
 // Copies the selected prompt K/V rows into the cache slots.
 cudaError_t prefill_gather(const void* K, const void* V, int rows, int T, int d, int k,
                            const int32_t* pos, void* Kc, void* Vc, cudaStream_t stream);

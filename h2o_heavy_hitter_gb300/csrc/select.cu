@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const float* __r
                                                                int stride,
                                                                const int32_t* __restrict__ lens,
                                                                int heads, int h, int r, int k,
+                                                               bool ring,
                                                                float* __restrict__ score,
                                                                int32_t* __restrict__ pos,
                                                                int32_t* __restrict__ meta,
@@ -132,19 +133,31 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const float* __r
   }
   int total;
   int s = block_exclusive_scan(kept, wsum, &total);
+  if (ring) {  // every slot empty first: the window's slots need not be contiguous
+    for (int j = tid; j < k; j += nt) {
+      ps[j] = -1;
+      sc[j] = 0.f;
+    }
+    __syncthreads();
+  }
   {
+    // Kept tokens in ascending position order take slots 0, 1, ...; in the
+    // ring layout the window's tokens (all after the older kept ones) take
+    // slot h + p mod r instead.
     int e = eq_base;
     for (int p = p0; p < p1; ++p)
       if (keep(p, e)) {
-        ps[s] = p;
-        sc[s] = cs[p];
+        const int slot = ring && p >= T - r ? h + p % r : s;
+        ps[slot] = p;
+        sc[slot] = cs[p];
         ++s;
       }
   }
-  for (int j = total + tid; j < k; j += nt) {
-    ps[j] = -1;
-    sc[j] = 0.f;
-  }
+  if (!ring)
+    for (int j = total + tid; j < k; j += nt) {
+      ps[j] = -1;
+      sc[j] = 0.f;
+    }
   if (tid == 0) {
     int32_t* mr = meta + static_cast<size_t>(row) * 4;
     mr[0] = total;
@@ -232,11 +245,11 @@ __global__ void reset_kernel(int rows, int k, float* __restrict__ score, int32_t
 }  // namespace
 
 cudaError_t prefill_select(const float* colsum, int rows, int T, const int32_t* lens, int heads,
-                           int h, int r, float* score, int32_t* pos, int32_t* meta, int32_t* err,
-                           cudaStream_t stream) {
+                           int h, int r, bool ring, float* score, int32_t* pos, int32_t* meta,
+                           int32_t* err, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  select_kernel<<<rows, kSelectThreads, 0, stream>>>(colsum, T, lens, heads, h, r, h + r, score,
-                                                     pos, meta, err);
+  select_kernel<<<rows, kSelectThreads, 0, stream>>>(colsum, T, lens, heads, h, r, h + r, ring,
+                                                     score, pos, meta, err);
   return cudaGetLastError();
 }
 

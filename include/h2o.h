@@ -56,6 +56,7 @@ extern "C" {
 
 #define H2O_KV_BF16 0  /* cache keys and values stored as bf16 (h2o_create) */
 #define H2O_KV_FP8 1   /* cache keys and values stored as E4M3 codes with per-token scales */
+#define H2O_LAYOUT_RING 0x100 /* OR into kv_format: heavy slots, then the window as a circular queue */
 
 typedef struct h2o_ctx h2o_ctx; /* opaque; created by h2o_create, freed by h2o_destroy */
 
@@ -95,6 +96,16 @@ int h2o_create(int layers, int batch, int heads, int head_dim, int h, int r, h2o
  * (h2o_cache_scales), 2d + 8 bytes per slot instead of 4d.
  * kv_format H2O_KV_BF16 is h2o_create. Other arguments and errors as for
  * h2o_create; an unknown kv_format gives H2O_EINVAL.
+ *
+ * kv_format H2O_KV_BF16 | H2O_LAYOUT_RING (needs r >= 1) lays each row's
+ * slots out as the pages' implementation does ([H2O] A, System Details: a
+ * heavy-hitter region and the recent tokens in a circular queue): heavy slots
+ * [0, h) in use from slot 0, and the token at recent position p in slot
+ * h + p mod r. The decode step then reads no position of a recent slot (they
+ * follow from t); its candidates are the heavy slots and the token leaving
+ * the window, which moves into the heavy slot it displaces. Results are those
+ * of the default slot-indexed layout (outputs, evictions, retained sets);
+ * only the slot order differs. h2o_decode_steps takes one launch per step.
  */
 int h2o_create_ex(int layers, int batch, int heads, int head_dim, int h, int r, int kv_format,
                   h2o_ctx** out);

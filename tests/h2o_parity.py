@@ -104,19 +104,34 @@ def _fp8_token(bits):
     return oracle.kv_fp8.quantize_vector(bf16_bits_to_f64(bits))
 
 
+def _slots_of(pos: np.ndarray, k: int, t_next: int, ring: tuple | None) -> np.ndarray:
+    """Cache slot of each retained position (ascending): slot-indexed, slots
+    0, 1, ...; ring layout (h, r): positions before the window t_next - r from
+    slot 0, window position p in slot h + p mod r."""
+    if ring is None:
+        return np.arange(len(pos))
+    h, r = ring
+    slots = np.empty(len(pos), dtype=np.int64)
+    old = pos < t_next - r
+    slots[old] = np.arange(int(old.sum()))
+    slots[~old] = h + pos[~old] % r
+    return slots
+
+
 def _resync_row(view, gpu_rows, pos: np.ndarray, scores: np.ndarray, k_bits, v_bits, k: int,
-                t_next: int, scales=None):
+                t_next: int, scales=None, ring: tuple | None = None):
     """Overwrite GPU rows (every copy of one checked row) with the oracle's
-    retained set, slots in ascending position order (with ``scales``, the
-    views of an FP8 cache's scales, the tokens are stored as the oracle
-    quantises them)."""
+    retained set, slots in ascending position order, or in the ring layout's
+    places with ``ring`` = (h, r) (with ``scales``, the views of an FP8 cache's
+    scales, the tokens are stored as the oracle quantises them)."""
     n = len(pos)
     dev = view["pos"].device
     rows_t = torch.as_tensor(np.atleast_1d(gpu_rows), device=dev, dtype=torch.long)
+    slots = _slots_of(np.asarray(pos), k, t_next, ring)
     pos_full = np.full(k, -1, dtype=np.int32)
-    pos_full[:n] = pos
+    pos_full[slots] = pos
     sc_full = np.zeros(k, dtype=np.float32)
-    sc_full[:n] = scores
+    sc_full[slots] = scores
     view["pos"][rows_t] = torch.from_numpy(pos_full).to(dev)
     view["score"][rows_t] = torch.from_numpy(sc_full).to(dev)
     if scales is not None:
@@ -124,7 +139,7 @@ def _resync_row(view, gpu_rows, pos: np.ndarray, scores: np.ndarray, k_bits, v_b
         vc = np.zeros_like(kc)
         ks = np.zeros(k, dtype=np.float32)
         vs = np.zeros(k, dtype=np.float32)
-        for i, p_ in enumerate(pos):
+        for i, p_ in zip(slots, pos):
             kc[i], ks[i] = _fp8_token(k_bits[p_])
             vc[i], vs[i] = _fp8_token(v_bits[p_])
         view["K"][rows_t] = torch.from_numpy(kc).to(dev)
@@ -135,8 +150,9 @@ def _resync_row(view, gpu_rows, pos: np.ndarray, scores: np.ndarray, k_bits, v_b
         kk = torch.zeros((k, k_bits.shape[1]), dtype=torch.bfloat16, device=dev)
         vv = torch.zeros_like(kk)
         if n:
-            kk[:n] = _to_bf16(k_bits[pos], dev)
-            vv[:n] = _to_bf16(v_bits[pos], dev)
+            idx = torch.as_tensor(slots, device=dev)
+            kk[idx] = _to_bf16(k_bits[pos], dev)
+            vv[idx] = _to_bf16(v_bits[pos], dev)
         view["K"][rows_t] = kk
         view["V"][rows_t] = vv
     view["meta"][rows_t] = torch.tensor([n, t_next, -1, 0], dtype=torch.int32, device=dev)
@@ -229,7 +245,8 @@ def _check_multi(rep, h2o, ctx, view, check, traces, qs, ks, vs, copies, set_che
 def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool = False,
                set_check_every: int = 1, workers: int | None = None,
                row_block: int | None = None, traces: list | None = None,
-               kv: str = "bf16", lens: list | None = None, decode: str = "step") -> Report:
+               kv: str = "bf16", lens: list | None = None, decode: str = "step",
+               layout: str = "slots") -> Report:
     """Runs one layer of workload ``w`` on the GPU and compares with the oracle.
 
     ``rows``: (b, head) pairs checked against the oracle (default: all).
@@ -242,7 +259,8 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
     after each) or "multi" (all steps in one h2o_decode_steps call, checked
     afterwards from the per-step outputs and evicted positions; a row whose
     eviction differs from the oracle's at a near-tie is counted and no longer
-    compared, since nothing can be resynchronised inside the call)."""
+    compared, since nothing can be resynchronised inside the call).
+    ``layout``: "slots" or "ring" (h2o_create's cache layout)."""
     import h2o_heavy_hitter_gb300 as h2o
 
     B, H, d, T, S, k = w.batch, w.heads, w.head_dim, w.prompt, w.steps, w.k
@@ -285,7 +303,8 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
 
     rep = Report(rows=len(check), steps=S)
     fp8 = kv == "fp8"
-    ctx = h2o.h2o_create(1, B, H, d, w.h, w.r, kv=kv)
+    ctx = h2o.h2o_create(1, B, H, d, w.h, w.r, kv=kv, layout=layout)
+    ring = (w.h, w.r) if layout == "ring" else None
     try:
         if lens is None:
             out = h2o.h2o_prefill(ctx, 0, Qd[:, :, :T].contiguous(), Kd[:, :, :T].contiguous(),
@@ -320,7 +339,7 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
                     rep.resyncs += 1
                     _, kb, vb = row_bits[ti]
                     _resync_row(view, copies_of(g, ti), tr["kept"], tr["kept_scores"], kb, vb, k,
-                                Tb[g // H], scales)
+                                Tb[g // H], scales, ring)
                 else:
                     rep.mismatches.append((-1, g, gp.tolist(), tr["kept"].tolist(), tr["margin"]))
             else:
@@ -373,7 +392,7 @@ def run_parity(w: Workload, layer: int = 0, rows: list | None = None, tile: bool
                         rep.resyncs += 1
                         _, kb, vb = row_bits[ti]
                         _resync_row(view, copies_of(g, ti), tr["kept_after"][s], tr["scores_after"][s],
-                                    kb, vb, k, Tb[g // H] + s + 1, scales)
+                                    kb, vb, k, Tb[g // H] + s + 1, scales, ring)
                         continue
                     rep.mismatches.append((s, g, int(ev[g]), int(tr["evicted"][s]), margin))
                     continue

@@ -188,7 +188,8 @@ def kv_cache_bytes(layers: int, hidden: int, batch: int, seq: int, bytes_per_ele
     return 2 * layers * hidden * batch * seq * bytes_per_elem
 
 
-def decode_bytes_per_row_step(k: int, d: int, kv: str = "bf16") -> int:
+def decode_bytes_per_row_step(k: int, d: int, kv: str = "bf16", layout: str = "slots",
+                              h: int | None = None) -> int:
     """Algorithmic HBM bytes of one decode step of one (layer, b, head) row.
 
     Reads: the k cached K and V rows (bf16, 4kd), the k accumulated scores
@@ -197,9 +198,15 @@ def decode_bytes_per_row_step(k: int, d: int, kv: str = "bf16") -> int:
     position and score (8), and the fp32 output (4d).
     With an FP8 cache (kv="fp8") a slot holds E4M3 codes (2kd for K and V)
     plus two fp32 scales (8k read), and the new slot is written as 2d code
-    bytes plus 8 scale bytes."""
+    bytes plus 8 scale bytes.
+    Ring layout (layout="ring", h heavy slots): positions are read for the h
+    heavy slots only (4h instead of 4k), and the token leaving the recent
+    window moves into the heavy slot it displaces (4d read, 4d + 8 written;
+    counted every step, an upper bound)."""
     if kv == "fp8":
         return 2 * k * d + 8 * k + 12 * k + 6 * d + 2 * d + 16 + 4 * d
+    if layout == "ring":
+        return 4 * k * d + 8 * k + 4 * h + 6 * d + 4 * d + 8 + 4 * d + 8 * d + 8
     return 4 * k * d + 12 * k + 6 * d + 4 * d + 8 + 4 * d
 
 
