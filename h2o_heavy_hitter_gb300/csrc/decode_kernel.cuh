@@ -217,9 +217,10 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   auto occ_g = [&](int gi) -> bool { return gi < nh || (gi >= a.h && gi < a.h + nring); };
   // slot s0 + i of this segment holds a token (a batch may reach past the
   // segment's last slot: those lanes loaded nothing)
+  const bool ring_full = RING && count >= a.k;  // every slot in use: no per-slot test
   auto occ = [&](int i) -> bool {
     if constexpr (RING)
-      return i < cap && occ_g(s0 + i);
+      return i < cap && (ring_full || occ_g(s0 + i));
     else
       return i < n;
   };
@@ -481,7 +482,7 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   int bslot = -1;
 #pragma unroll 1
   for (int jj = 0, i = tid; i < slot_end; ++jj, i += NT) {
-    if (RING && !occ_g(i)) continue;
+    if (RING && !ring_full && !occ_g(i)) continue;
     float sc;
     int ps;
     if (solo && jj < kSoloRegs) {
