@@ -20,7 +20,8 @@ import torch
 __all__ = [
     "H2OError", "H2OContext", "load_library", "h2o_create", "h2o_destroy", "h2o_prefill",
     "h2o_decode_step", "h2o_decode_steps", "h2o_prefill_attention", "h2o_cache_positions", "h2o_last_evicted",
-    "h2o_cache_view", "h2o_cache_scales", "h2o_sync_check", "LIB_PATH", "KV_FORMATS",
+    "h2o_cache_view", "h2o_cache_scales", "h2o_sync_check", "h2o_test_wait_limit", "LIB_PATH",
+    "KV_FORMATS",
 ]
 
 LIB_PATH = Path(__file__).resolve().parent / "libh2o.so"
@@ -65,6 +66,7 @@ def load_library() -> ctypes.CDLL:
                                ctypes.POINTER(P), ctypes.POINTER(P)]),
         "h2o_cache_dims": (I, [P, ctypes.POINTER(I), ctypes.POINTER(I)]),
         "h2o_sync_check": (I, [P]),
+        "h2o_test_wait_limit": (I, [P]),
         "h2o_last_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -288,6 +290,12 @@ def h2o_cache_scales(ctx: H2OContext, layer: int) -> dict:
     dev = torch.device("cuda", torch.cuda.current_device())
     mk = lambda p: torch.as_tensor(_DeviceArray(p.value, (ctx.rows, ctx.k), "<f4"), device=dev)
     return {"K": mk(ptrs[0]), "V": mk(ptrs[1])}
+
+
+def h2o_test_wait_limit(ctx: H2OContext) -> None:
+    """Enqueues a kernel whose bounded wait runs out (the failure path on demand);
+    the next h2o_sync_check raises H2O_EDEVICE."""
+    _check(load_library().h2o_test_wait_limit(ctypes.c_void_p(ctx.handle)))
 
 
 def h2o_sync_check(ctx: H2OContext) -> None:

@@ -468,6 +468,13 @@ int h2o_cache_dims(h2o_ctx* c, int* k, int* rows) {
   return H2O_OK;
 }
 
+int h2o_test_wait_limit(h2o_ctx* c) {
+  if (!c) return fail(H2O_EINVAL, "null context");
+  cudaError_t e = h2o::wait_limit_probe(c->err, current_stream());
+  if (e != cudaSuccess) return cuda_fail(e, "wait-limit probe launch");
+  return H2O_OK;
+}
+
 int h2o_sync_check(h2o_ctx* c) {
   if (!c) return fail(H2O_EINVAL, "null context");
   cudaStream_t s = current_stream();

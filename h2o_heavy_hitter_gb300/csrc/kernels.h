@@ -120,5 +120,8 @@ cudaError_t prefill_gather_fp8(const void* K, const void* V, int rows, int T, in
                                float* vscale, cudaStream_t stream);
 cudaError_t cache_reset(int rows, int k, float* score, int32_t* pos, int32_t* meta,
                         cudaStream_t stream);
+// One kernel whose bounded wait is never satisfied: it gives up after the
+// wait limit and sets kErrWaitTimeout in *err (the failure path, on demand).
+cudaError_t wait_limit_probe(int32_t* err, cudaStream_t stream);
 
 }  // namespace h2o

@@ -242,7 +242,23 @@ __global__ void reset_kernel(int rows, int k, float* __restrict__ score, int32_t
   }
 }
 
+// Failure-path probe: waits, with the library's bounded wait, on an mbarrier
+// nothing ever arrives on. The wait gives up after the limit, sets the wait
+// bit of the error word and the kernel returns, as a kernel of the hot path
+// would when a producer never delivers.
+__global__ void wait_limit_kernel(int32_t* err) {
+  __shared__ uint64_t bar;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  mbar_wait(&bar, 0, err);
+}
+
 }  // namespace
+
+cudaError_t wait_limit_probe(int32_t* err, cudaStream_t stream) {
+  wait_limit_kernel<<<1, 1, 0, stream>>>(err);
+  return cudaGetLastError();
+}
 
 cudaError_t prefill_select(const float* colsum, int rows, int T, const int32_t* lens, int heads,
                            int h, int r, bool ring, float* score, int32_t* pos, int32_t* meta,

@@ -291,6 +291,17 @@ int h2o_cache_scales(h2o_ctx* ctx, int layer, float** k_scale, float** v_scale);
 int h2o_cache_dims(h2o_ctx* ctx, int* k, int* rows);
 
 /*
+ * h2o_test_wait_limit - the failure path on demand: enqueues one kernel whose
+ * bounded mbarrier wait is never satisfied (nothing arrives on the barrier).
+ * Like any kernel of the library whose producer never delivers, it gives up
+ * after the wait limit (2 s), sets bit 1 (wait timeout) of the context's
+ * device error word and returns; no kernel traps. The next h2o_sync_check
+ * reports H2O_EDEVICE and clears the word, and the context stays usable.
+ * Errors: H2O_EINVAL, H2O_ECUDA.
+ */
+int h2o_test_wait_limit(h2o_ctx* ctx);
+
+/*
  * h2o_sync_check - synchronise the current stream and report, then clear, the
  * context's device error word. Errors: H2O_ECUDA, H2O_EDEVICE.
  */
