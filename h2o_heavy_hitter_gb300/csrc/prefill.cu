@@ -792,19 +792,17 @@ __global__ void __launch_bounds__(kColThreads, 1)
             a2[(c4 >> 2) & 3] = f2_add(a2[(c4 >> 2) & 3], f2_add(f2_pack(x[0], x[1]), f2_pack(x[2], x[3])));
           }
         } else {
+          float a4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int c4 = 0; c4 < kColCols; c4 += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(L + c4);
-            float x0, x1, x2, x3;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c4]), __uint_as_float(s[c4 + 1])), sc2,
-                             f2_pack(l4.x, l4.y)),
-                      x0, x1);
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c4 + 2]), __uint_as_float(s[c4 + 3])), sc2,
-                             f2_pack(l4.z, l4.w)),
-                      x2, x3);
-            a2[(c4 >> 2) & 3] = f2_add(a2[(c4 >> 2) & 3],
-                                       f2_add(f2_pack(ex2(x0), ex2(x1)), f2_pack(ex2(x2), ex2(x3))));
+            a4[0] += ex2(fmaf(__uint_as_float(s[c4]), p.qscale, l4.x));
+            a4[1] += ex2(fmaf(__uint_as_float(s[c4 + 1]), p.qscale, l4.y));
+            a4[2] += ex2(fmaf(__uint_as_float(s[c4 + 2]), p.qscale, l4.z));
+            a4[3] += ex2(fmaf(__uint_as_float(s[c4 + 3]), p.qscale, l4.w));
           }
+          a2[0] = f2_pack(a4[0], a4[1]);
+          a2[1] = f2_pack(a4[2], a4[3]);
         }
         float a8[8];
 #pragma unroll
