@@ -89,16 +89,34 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const float* __r
         if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
       }
       __syncthreads();
-      if (tid == 0) {
-        int cum = 0;
-        for (int b = 0; b < 256; ++b) {
-          const int c = static_cast<int>(hist[b]);
-          if (cum + c > rank) {
-            s_prefix = prefix | (static_cast<unsigned>(b) << shift);
-            s_rank = rank - cum;
-            break;
+      if (tid < 32) {
+        // Warp 0 finds the bin holding the rank-th key: each lane sums eight
+        // bins, a shuffle scan places the lanes, and the one lane whose range
+        // contains the rank walks its eight bins.
+        unsigned c[8];
+        int local = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          c[j] = hist[tid * 8 + j];
+          local += static_cast<int>(c[j]);
+        }
+        int incl = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, off);
+          if (tid >= off) incl += y;
+        }
+        int cum = incl - local;
+        if (cum <= rank && rank < incl) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (cum + static_cast<int>(c[j]) > rank) {
+              s_prefix = prefix | (static_cast<unsigned>(tid * 8 + j) << shift);
+              s_rank = rank - cum;
+              break;
+            }
+            cum += static_cast<int>(c[j]);
           }
-          cum += c;
         }
       }
       __syncthreads();
