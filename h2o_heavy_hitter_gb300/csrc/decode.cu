@@ -43,21 +43,22 @@ DecodeConfig decode_config(int rows, int k, int d, int num_sms, const DecodeTuni
   c.pdl = tune.pdl >= 0;
   // Measured on GB300 (decode sweeps over the workload shapes):
   //  * many rows (>= 4 per SM): one 128-thread CTA per row, one batch in flight;
-  //  * one to four rows per SM: one 256-thread CTA per row with two batches in
-  //    flight per group (software pipelining), which keeps memory busy across
-  //    the serial batches of a long row;
-  //  * fewer rows than SMs: rows split into segments of 128-thread CTAs until
-  //    the grid covers every SM about eight times.
-  c.threads = tune.threads == 128 || tune.threads == 256
-                  ? tune.threads
-                  : (few_rows || many_rows ? 128 : 256);
-  c.pipe = tune.pipe > 0 || (tune.pipe == 0 && !few_rows && !many_rows);
+  //  * fewer rows than that: 256-thread CTAs with two batches in flight per
+  //    group (software pipelining), which keeps memory busy across the serial
+  //    batches of a long row; below one row per SM the rows are split into
+  //    segments until the grid is one wave of about two CTAs per SM (128 rows
+  //    of 4096 slots: 49 us per step with two segments per row, against 61 us
+  //    for eight segments of 128-thread CTAs and 61 us for three).
+  // Short rows (under 256 slots) are latency-bound: 128 threads, one batch.
+  const bool small = many_rows || (few_rows && k < 256);
+  c.threads = tune.threads == 128 || tune.threads == 256 ? tune.threads : (small ? 128 : 256);
+  c.pipe = tune.pipe > 0 || (tune.pipe == 0 && !small);
   const int groups = c.threads / (d / 8);
   int segs = 1;
   if (tune.segs > 0) {
     segs = tune.segs;
   } else if (few_rows) {
-    while (segs < kMaxDecodeSegs && static_cast<long>(rows) * segs < 8L * num_sms &&
+    while (segs < kMaxDecodeSegs && static_cast<long>(rows) * segs * 2 <= 2L * num_sms &&
            (k + 2 * segs - 1) / (2 * segs) >= 2 * groups * c.unroll)
       segs *= 2;
   }

@@ -197,7 +197,9 @@ int h2o_decode_step(h2o_ctx* ctx, int layer, const void* q, const void* k_new, c
  * position evicted by each row at each step (-1: none, the new token's own
  * position when it is dropped), or NULL. With h + r <= 8192 all steps run in
  * one launch, one CTA per row looping over its steps (no per-step launch and
- * drain); larger budgets take one launch per step. steps >= 0 (0: nothing is
+ * drain); larger budgets, and rows of 1024 slots or more when there are fewer
+ * rows than SMs (where splitting rows over several CTAs moves the bytes
+ * faster), take one launch per step. steps >= 0 (0: nothing is
  * done). Allocates nothing and never synchronises; capturable in a CUDA
  * graph. Errors: H2O_EINVAL, H2O_ESTATE (layer never prefilled), H2O_ECUDA.
  */
