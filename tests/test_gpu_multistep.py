@@ -24,6 +24,7 @@ MULTI = [
     ("h0-recent-only", 1, 2, 128, 200, 30, 0, 24),
     ("empty-prompt", 1, 2, 64, 0, 30, 6, 4),
     ("budget-over-8192-per-step-launches", 1, 1, 64, 8300, 8, 4100, 4100),
+    ("few-long-rows-per-step-launches", 1, 2, 64, 1300, 12, 600, 600),  # rows split over CTAs
 ]
 
 

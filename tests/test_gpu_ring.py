@@ -35,6 +35,12 @@ def test_ring_layout_matches_oracle(name, B, H, d, T, S, h, r):
     _assert_ok(run_parity(w, layout="ring"), name)
 
 
+def test_ring_layout_multistep_call_matches_oracle():
+    """h2o_decode_steps on a ring cache (one launch per step inside the call)."""
+    w = Workload(622, "ring-multi", 1, 2, 2, 128, 180, 30, 20, 12, 0.8)
+    _assert_ok(run_parity(w, layout="ring", decode="multi"), "ring-multi")
+
+
 def test_ring_layout_ragged_batch_matches_oracle():
     lens = [300, 0, 7, 130, 257]
     w = Workload(620, "ring-ragged", 1, len(lens), 2, 128, 300, 30, 20, 12, 0.8)
