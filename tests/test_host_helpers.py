@@ -1,0 +1,46 @@
+"""Host-side helpers shared by the tests and the bench (CPU only)."""
+import numpy as np
+
+from h2o_parity import _slots_of
+from workloads import bf16_bits_to_f32, decode_bytes_per_row_step, stream_chunk
+
+
+def test_stream_chunks_are_reproducible_and_independent():
+    a = stream_chunk(7, 3, 64, 4, 64)
+    b = stream_chunk(7, 3, 64, 4, 64)
+    c = stream_chunk(7, 4, 64, 4, 64)
+    assert all(x.shape == (64, 4, 64) and x.dtype == np.uint16 for x in a)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
+    assert not any(np.array_equal(x, y) for x, y in zip(a, c))
+
+
+def test_stream_chunk_queries_lean_on_one_direction():
+    """Queries carry +2 u along one unit direction shared by every chunk, so
+    their mean is about 2 u (2 in norm) while the values have mean about 0."""
+    q0, _, v0 = (bf16_bits_to_f32(x).reshape(-1, 64) for x in stream_chunk(1, 0, 2048, 2, 64))
+    q1 = bf16_bits_to_f32(stream_chunk(1, 1, 2048, 2, 64)[0]).reshape(-1, 64)
+    m0, m1 = q0.mean(axis=0), q1.mean(axis=0)
+    assert abs(np.linalg.norm(m0) - 2.0) < 0.1
+    assert np.dot(m0, m1) / (np.linalg.norm(m0) * np.linalg.norm(m1)) > 0.99
+    assert np.linalg.norm(v0.mean(axis=0)) < 0.2
+
+
+def test_ring_slots_of_retained_positions():
+    """Ring layout: positions before the window fill slots 0.. in order; window
+    position p sits in slot h + p mod r."""
+    pos = np.array([1, 5, 9, 16, 17, 18, 19])
+    slots = _slots_of(pos, k=7, t_next=20, ring=(3, 4))
+    assert slots.tolist() == [0, 1, 2, 3, 4, 5, 6]
+    pos = np.array([2, 13, 14, 15, 16])  # window 13..16 of t_next = 17
+    assert _slots_of(pos, k=7, t_next=17, ring=(3, 4)).tolist() == [0, 4, 5, 6, 3]
+    assert _slots_of(pos, k=7, t_next=17, ring=None).tolist() == [0, 1, 2, 3, 4]
+
+
+def test_decode_byte_model_of_the_layouts():
+    k, d, h = 460, 128, 230
+    slots = decode_bytes_per_row_step(k, d)
+    ring = decode_bytes_per_row_step(k, d, "bf16", "ring", h)
+    assert slots == 4 * k * d + 12 * k + 14 * d + 8
+    # the ring layout reads h positions instead of k and moves one token (8d + 8)
+    assert ring - slots == 4 * h - 4 * k + 8 * d + 8
+    assert decode_bytes_per_row_step(k, d, "fp8") == 2 * k * d + 20 * k + 12 * d + 16
