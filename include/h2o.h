@@ -276,7 +276,10 @@ int h2o_last_evicted(h2o_ctx* ctx, int layer, int32_t* host_pos);
  * h2o_create). The library keeps ownership; the addresses stay valid until
  * h2o_destroy. A caller may write through them (between calls, on the same
  * stream) to install a cache state; the fill count in meta must then match the
- * occupied slots. Any output pointer may be NULL. Errors: H2O_EINVAL.
+ * occupied slots, which are slots 0 .. filled-1 of the slot-indexed layout, or
+ * for H2O_LAYOUT_RING the tokens older than the window from slot 0 and window
+ * position p in slot h + p mod r. Any output pointer may be NULL.
+ * Errors: H2O_EINVAL.
  */
 int h2o_cache_view(h2o_ctx* ctx, int layer, void** K, void** V, float** score, int32_t** pos,
                    int32_t** meta);
