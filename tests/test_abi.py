@@ -68,3 +68,28 @@ def test_misaligned_prompt_buffers_are_rejected_without_gpu(lib):
     assert b"16-byte aligned" in lib.h2o_last_error()
     assert lib.h2o_prefill_attention_noalloc(bad, good, good, 2, 256, 128, good, good, None) == -1
     assert b"16-byte aligned" in lib.h2o_last_error()
+
+
+def test_new_entry_points_check_arguments_without_gpu(lib):
+    """Argument checks of the ragged prefill, the multi-step decode, the ring
+    layout and the failure probe run before any CUDA call."""
+    P, I = ctypes.c_void_p, ctypes.c_int
+    lib.h2o_last_error.restype = ctypes.c_char_p
+    lib.h2o_prefill_ragged.argtypes = [P, I, P, P, P, I, P, P]
+    assert lib.h2o_prefill_ragged(None, 0, None, None, None, 16, None, None) == -1
+    assert b"null lens" in lib.h2o_last_error()
+    fake = 0x10000  # never dereferenced: the context check fails first
+    assert lib.h2o_prefill_ragged(None, 0, fake, fake, fake, 16, fake, fake) == -1
+    assert b"null context" in lib.h2o_last_error()
+    lib.h2o_decode_steps.argtypes = [P, I, I, P, P, P, P, P]
+    assert lib.h2o_decode_steps(None, 0, 4, None, None, None, None, None) == -1
+    lib.h2o_test_wait_limit.argtypes = [P]
+    assert lib.h2o_test_wait_limit(None) == -1
+    lib.h2o_create_ex.argtypes = [I] * 7 + [ctypes.POINTER(P)]
+    out = P()
+    ring = 0x100
+    assert lib.h2o_create_ex(1, 1, 1, 64, 4, 0, ring, ctypes.byref(out)) == -1  # no window
+    assert b"H2O_LAYOUT_RING" in lib.h2o_last_error()
+    assert lib.h2o_create_ex(1, 1, 1, 64, 4, 4, 1 | ring, ctypes.byref(out)) == -1  # FP8 + ring
+    assert lib.h2o_create_ex(1, 1, 1, 64, 4, 4, 7, ctypes.byref(out)) == -1  # unknown format
+    assert out.value is None
