@@ -285,6 +285,7 @@ class RowTrace:
     margins: list = field(default_factory=list)
     kept_after: list = field(default_factory=list)
     scores_after: list = field(default_factory=list)
+    evicted_scores: list = field(default_factory=list)  # score the evicted token held (0 if none)
 
 
 def run_row(q_all, k_all, v_all, T: int, S: int, h: int, r: int,
@@ -302,6 +303,7 @@ def run_row(q_all, k_all, v_all, T: int, S: int, h: int, r: int,
         tr.outs.append(lg.out)
         tr.evicted.append(lg.evicted)
         tr.margins.append(lg.margin)
+        tr.evicted_scores.append(lg.evicted_score)
         if keep_sets:
             tr.kept_after.append(c.pos.copy())
             tr.scores_after.append(c.score.copy())

@@ -39,6 +39,19 @@ MUTANTS = {
                                   "np.lexsort((-cand, colsum[:n_cand]))"),
     "prefill scale ignored": ("S = scale * (Q[i0:i1] @ K[:i1].T)", "S = (Q[i0:i1] @ K[:i1].T)"),
     "prefill values from keys": ("O[i0:i1] = P @ V[:i1]", "O[i0:i1] = P @ K[:i1, :V.shape[1]]"),
+    # the near-tie margin (steps below the threshold are excused from exact comparison)
+    "decode margin forced to zero": ("margin = (s2 - s1) / s2 if s2 > 0 else 0.0", "margin = 0.0"),
+    "prefill margin forced to zero": ("margin = (s_keep - s_drop) / s_keep if s_keep > 0 else 0.0",
+                                      "margin = 0.0"),
+    "decode margin over every attended token": ("s1, s2 = score[order[0]], score[order[1]]",
+                                                "s1, s2 = np.sort(score)[:2]"),
+    "decode margin not relative": ("margin = (s2 - s1) / s2 if s2 > 0 else 0.0",
+                                   "margin = (s2 - s1) if s2 > 0 else 0.0"),
+    "prefill margin against the wrong dropped key": ("s_drop = colsum[order[n_drop - 1]]",
+                                                     "s_drop = colsum[order[max(n_drop - 2, 0)]]"),
+    "prefill margin relative to the dropped key": (
+        "margin = (s_keep - s_drop) / s_keep if s_keep > 0 else 0.0",
+        "margin = (s_keep - s_drop) / s_drop if s_drop > 0 else 0.0"),
 }
 
 

@@ -12,7 +12,11 @@
 (d) brute force on tiny inputs: prefill keeps the max-sum subset (ties to later
     positions) and every decode eviction is the exhaustive minimum;
 (e) the budget-3 illustration of the H2O summary page (section 4.1);
-(f) the 180 GB sizing example of the H2O summary page (section 1).
+(f) the 180 GB sizing example of the H2O summary page (section 1);
+(g) the near-tie margin that decides which eviction decisions are excused
+    from bit-exact comparison: exact values on hand-built decode and prefill
+    cases where a token outside the candidate set would change the answer, and
+    a recomputation by plain loops over the candidates on tiny random inputs.
 """
 import itertools
 import json
@@ -253,6 +257,95 @@ def check_f_kv_cache_sizing_example(oracle):
     assert round(b / 1e9) == g["expected_gb"]
 
 
+# ----------------------------------------------------------------------------- (g)
+# The margin of an eviction is (s2 - s1) / s2 between the evicted key s1 and the
+# runner-up s2 among the candidates (positions <= t - r); at prefill it is
+# (s_keep - s_drop) / s_keep between the smallest kept and the largest dropped
+# heavy-hitter candidate. Steps whose margin is below the near-tie threshold are
+# the only ones whose decisions may differ from the GPU's, so the margin must be
+# right: too small and real mismatches are excused, too large and none are.
+def check_g_decode_margin_hand_built(oracle):
+    d = 4
+    K = np.zeros((5, d))
+    V = np.eye(5, d)
+    # zero query: every one of the 5 attended tokens gets p = 0.2
+    c = oracle.RowCache(h=3, r=1, scale=1.0, pos=np.array([0, 1, 2, 3]), K=K[:4].copy(),
+                        V=V[:4].copy(), score=np.array([0.7, 0.2, 0.25, 0.1]), t=4)
+    lg = oracle.decode_step(c, np.zeros(d), K[4], V[4])
+    # candidates (positions <= 3) after accumulation: 0.9, 0.4, 0.45, 0.3; the new
+    # token (position 4, score 0.2, the smallest of all) is not a candidate
+    assert lg.evicted == 3 and lg.n_candidates == 4
+    assert abs(lg.evicted_score - 0.3) < 1e-15
+    assert abs(lg.margin - (0.4 - 0.3) / 0.4) < 1e-12
+    # with r = 2 position 3 is protected as well: candidates 0.9, 0.4, 0.45
+    c = oracle.RowCache(h=2, r=2, scale=1.0, pos=np.array([0, 1, 2, 3]), K=K[:4].copy(),
+                        V=V[:4].copy(), score=np.array([0.7, 0.2, 0.25, 0.1]), t=4)
+    lg = oracle.decode_step(c, np.zeros(d), K[4], V[4])
+    assert lg.evicted == 1 and lg.n_candidates == 3
+    assert abs(lg.margin - (0.45 - 0.4) / 0.45) < 1e-12
+    # a single candidate has no runner-up: no near-tie is possible
+    c = oracle.RowCache(h=0, r=1, scale=1.0, pos=np.array([3]), K=K[:1].copy(), V=V[:1].copy(),
+                        score=np.array([0.5]), t=4)
+    lg = oracle.decode_step(c, np.zeros(d), K[4], V[4])
+    assert lg.evicted == 3 and lg.margin == np.inf
+
+
+def check_g_prefill_margin_hand_built(oracle):
+    # T = 8, r = 2: candidates 0..5 with scores 1.0 0.5 0.8 0.6 2.0 0.9; the two
+    # recent tokens (0.3, 0.4) have the smallest scores but never compete
+    colsum = np.array([1.0, 0.5, 0.8, 0.6, 2.0, 0.9, 0.3, 0.4])
+    kept, margin = oracle.prefill_select(colsum, 2, 2)
+    np.testing.assert_array_equal(kept, [0, 4, 6, 7])
+    assert abs(margin - (1.0 - 0.9) / 1.0) < 1e-12
+    kept, margin = oracle.prefill_select(colsum, 3, 2)
+    np.testing.assert_array_equal(kept, [0, 4, 5, 6, 7])
+    assert abs(margin - (0.9 - 0.8) / 0.9) < 1e-12
+    kept, margin = oracle.prefill_select(colsum, 0, 2)  # nothing kept among candidates
+    assert margin == np.inf
+    kept, margin = oracle.prefill_select(colsum, 6, 2)  # T <= h + r: nothing dropped
+    assert margin == np.inf and len(kept) == 8
+
+
+def _margin_by_loops(keys):
+    """(s2 - s1) / s2 of the two smallest (score, position) keys, plain loops."""
+    first = second = None
+    for key in keys:
+        if first is None or key < first:
+            first, second = key, first
+        elif second is None or key < second:
+            second = key
+    if second is None:
+        return np.inf
+    return (second[0] - first[0]) / second[0] if second[0] > 0 else 0.0
+
+
+def check_g_margins_equal_recomputation_over_candidates(oracle, h, r):
+    w = SMALL.with_(head_dim=8, prompt=12, steps=16)
+    for seed in range(3):
+        q, k, v = _row(w, b=seed)
+        T, S = w.prompt, w.steps
+        pre = oracle.prefill(q[:T], k[:T], v[:T], h, r)
+        if T > h + r and h > 0:
+            cand = range(T - r)
+            kept_heavy = [j for j in cand if j in set(pre.kept.tolist())]
+            dropped = [j for j in cand if j not in set(pre.kept.tolist())]
+            s_keep = min(pre.colsum[j] for j in kept_heavy)
+            s_drop = max(pre.colsum[j] for j in dropped)
+            assert abs(pre.margin - (s_keep - s_drop) / s_keep) < 1e-12
+        c = pre.cache
+        for s in range(S):
+            t = T + s
+            lg = oracle.decode_step(c, q[t], k[t], v[t])
+            if lg.evicted < 0:
+                continue
+            after = dict(zip(c.pos.tolist(), c.score.tolist()))
+            after[lg.evicted] = lg.evicted_score
+            keys = [(after[p], p) for p in lg.pos_attended.tolist() if p <= t - r]
+            assert len(keys) == lg.n_candidates
+            m = _margin_by_loops(keys)
+            assert (m == np.inf and lg.margin == np.inf) or abs(lg.margin - m) < 1e-12
+
+
 # ----------------------------------------------------------------------------- inputs
 def test_bf16_rounding_matches_torch_round_to_nearest_even():
     rng = np.random.default_rng(0)
@@ -331,3 +424,16 @@ def test_e_budget_three_illustration():
 
 def test_f_kv_cache_sizing_example():
     check_f_kv_cache_sizing_example(_real_oracle)
+
+
+def test_g_decode_margin_hand_built():
+    check_g_decode_margin_hand_built(_real_oracle)
+
+
+def test_g_prefill_margin_hand_built():
+    check_g_prefill_margin_hand_built(_real_oracle)
+
+
+@pytest.mark.parametrize("h,r", [(3, 3), (4, 1), (2, 0), (1, 2)])
+def test_g_margins_equal_recomputation_over_candidates(h, r):
+    check_g_margins_equal_recomputation_over_candidates(_real_oracle, h, r)
