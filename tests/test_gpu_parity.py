@@ -1,9 +1,12 @@
 """GPU parity of the CUDA path (called through the C ABI) against the CPU oracle.
 
 Tolerances: outputs within 2e-2 max-abs and 2e-3 mean-abs of the fp64 oracle
-(bf16 inputs, fp32 accumulation); retained sets and evicted positions equal at
-every step whose oracle margin is at least 1e-4 (near-ties are counted and the
-GPU row is resynchronised to the oracle).
+(bf16 inputs, fp32 accumulation); accumulated scores of the retained tokens
+within 1e-4 relative; retained sets and evicted positions equal at every step
+whose oracle margin is at least 1e-4. Below that margin a differing decision
+is excused only if it is near-minimal under the oracle's scores (counted, and
+the GPU row is resynchronised to the oracle), and near-ties may make up at
+most 1 % of all decisions checked.
 """
 import gc
 
@@ -12,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from h2o_parity import MAX_ABS, MEAN_ABS, run_parity
+from h2o_parity import MAX_ABS, MEAN_ABS, assert_report, run_parity, run_parity_full
 from workloads import WORKLOADS, Workload, bf16_bits_to_f64, head_direction, row_tokens
 
 pytestmark = pytest.mark.gpu
@@ -23,16 +26,10 @@ def _h2o():
     return h2o
 
 
-def _assert_ok(rep, label):
-    print(f"\n[{label}] rows={rep.rows} steps={rep.steps} evict_checks={rep.evict_checks} "
-          f"set_checks={rep.set_checks} near_ties={rep.near_ties} "
-          f"near_tie_mismatches={rep.near_tie_mismatches} "
-          f"prefill max/mean={rep.prefill_max_abs:.2e}/{rep.prefill_mean_abs:.2e} "
-          f"decode max/mean={rep.decode_max_abs:.2e}/{rep.decode_mean_abs:.2e} "
-          f"score max rel={rep.score_max_rel:.2e}")
-    assert not rep.mismatches, rep.mismatches[:5]
-    assert rep.prefill_max_abs <= MAX_ABS and rep.prefill_mean_abs <= MEAN_ABS
-    assert rep.decode_max_abs <= MAX_ABS and rep.decode_mean_abs <= MEAN_ABS
+def _assert_ok(rep, label, **kw):
+    assert_report(rep, label, **kw)
+    if rep.rows and rep.steps and rep.evict_checks:
+        assert rep.score_checks > 0  # the accumulated scores were compared
 
 
 def test_tiny_workload_every_row():
@@ -155,32 +152,34 @@ def test_error_codes():
     ctx.close()
 
 
-# Full-size workloads in their real launch shape, checked on sampled rows: the
-# sampled rows are drawn exactly and repeated across the batch (rows are
-# independent), every copy must evict identically, and the first copy of each
-# sampled row is compared with the oracle at every step.
-def _sample(w, n, seed):
-    rng = np.random.default_rng(seed)
-    idx = rng.choice(w.batch * w.heads, size=n, replace=False)
-    return [(int(i) // w.heads, int(i) % w.heads) for i in sorted(idx)]
+# Full-size workloads, every row with its own seeded data, in the launch
+# configuration the benchmark times. The GPU runs first; the oracle then runs
+# every row in worker processes and each row is compared step by step
+# (h2o_parity.run_parity_full). A row is compared up to the step where a
+# near-tie decision differs (excused only if near-minimal), and such rows stay
+# rare: at most 1 % of the rows.
+def _assert_full(rep, label):
+    _assert_ok(rep, label)
+    assert rep.evict_checks > 0 and rep.score_checks >= rep.rows
+    assert rep.diverged_rows <= max(1, rep.rows // 100), rep.diverged_rows
 
 
-def test_batch_256_full_size_sampled_rows():
+def test_batch_256_every_row():
     w = WORKLOADS["batch-256"]
-    _assert_ok(run_parity(w, rows=_sample(w, 16, 5), tile=True, set_check_every=64), "batch-256")
+    _assert_full(run_parity_full(w, snap_every=128), "batch-256")
 
 
-def test_llama_7b_32k_full_size_sampled_rows():
+def test_llama_7b_32k_every_row():
     w = WORKLOADS["llama-7b-32k"]
-    _assert_ok(run_parity(w, rows=_sample(w, 4, 4), tile=True, set_check_every=128,
-                          row_block=2048), "llama-7b-32k")
+    _assert_full(run_parity_full(w, snap_every=128, row_block=512), "llama-7b-32k")
 
 
 @pytest.mark.parametrize("layer", [0, 47])
-def test_opt_30b_stack_full_size_sampled_layers(layer):
+def test_opt_30b_stack_every_row_of_first_and_last_layer(layer):
+    """Two of the 48 layers (each layer's inputs are independent draws, and the
+    layers run one after the other through the same kernels)."""
     w = WORKLOADS["opt-30b-stack"]
-    _assert_ok(run_parity(w, layer=layer, rows=_sample(w, 16, 30 + layer), tile=True,
-                          set_check_every=64), f"opt-30b-stack layer {layer}")
+    _assert_full(run_parity_full(w, layer=layer, snap_every=128), f"opt-30b-stack layer {layer}")
 
 
 def test_long_stream_soak_constant_memory():
