@@ -21,7 +21,8 @@ __all__ = [
     "H2OError", "H2OContext", "load_library", "h2o_create", "h2o_destroy", "h2o_prefill",
     "h2o_decode_step", "h2o_decode_steps", "h2o_prefill_attention", "h2o_cache_positions", "h2o_last_evicted",
     "h2o_cache_view", "h2o_cache_scales", "h2o_sync_check", "h2o_test_wait_limit", "LIB_PATH",
-    "KV_FORMATS",
+    "KV_FORMATS", "h2o_reset", "h2o_attention_sync_check", "h2o_attention_test_wait_limit",
+    "h2o_test_fail_allocations", "h2o_forget_device_state",
 ]
 
 LIB_PATH = Path(__file__).resolve().parent / "libh2o.so"
@@ -67,6 +68,11 @@ def load_library() -> ctypes.CDLL:
         "h2o_cache_dims": (I, [P, ctypes.POINTER(I), ctypes.POINTER(I)]),
         "h2o_sync_check": (I, [P]),
         "h2o_test_wait_limit": (I, [P]),
+        "h2o_reset": (I, [P, I]),
+        "h2o_attention_sync_check": (I, [P]),
+        "h2o_attention_test_wait_limit": (I, [P]),
+        "h2o_forget_device_state": (None, []),
+        "h2o_test_fail_allocations": (I, [I]),
         "h2o_last_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -186,6 +192,11 @@ def h2o_prefill(ctx: H2OContext, layer: int, Q, K, V, out=None, lens=None) -> to
     return out
 
 
+def h2o_reset(ctx: H2OContext, layer: int = -1) -> None:
+    """Empties one layer (or every layer with -1) for a new prompt."""
+    _check(load_library().h2o_reset(ctypes.c_void_p(ctx.handle), layer))
+
+
 def h2o_decode_step(ctx: H2OContext, layer: int, q, k_new, v_new, out=None) -> torch.Tensor:
     """One decode step of one layer; returns the fp32 output [B, H, d]."""
     shape = (ctx.batch, ctx.heads, ctx.head_dim)
@@ -300,3 +311,30 @@ def h2o_test_wait_limit(ctx: H2OContext) -> None:
 
 def h2o_sync_check(ctx: H2OContext) -> None:
     _check(load_library().h2o_sync_check(ctypes.c_void_p(ctx.handle)))
+
+
+def _stream_ptr(stream) -> int | None:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream or None
+
+
+def h2o_attention_sync_check(stream=None) -> None:
+    """Synchronises ``stream`` (default: the current stream) and raises
+    H2O_EDEVICE if a cache-free prefill call reported a device error."""
+    _check(load_library().h2o_attention_sync_check(_stream_ptr(stream)))
+
+
+def h2o_attention_test_wait_limit(stream=None) -> None:
+    """Enqueues a kernel whose bounded wait runs out against the library-level
+    error word; the next h2o_attention_sync_check raises H2O_EDEVICE."""
+    _check(load_library().h2o_attention_test_wait_limit(_stream_ptr(stream)))
+
+
+def h2o_test_fail_allocations(n: int) -> None:
+    """Makes the library's next ``n`` device allocations fail (0 ends it)."""
+    _check(load_library().h2o_test_fail_allocations(n))
+
+
+def h2o_forget_device_state() -> None:
+    """Drops the library's cached per-device state (after a device reset)."""
+    load_library().h2o_forget_device_state()

@@ -100,6 +100,13 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// Asks the TMA engine to pull `bytes` (multiple of 16; address 16-byte aligned)
+// of global memory into L2. Nothing is read into the SM, and L2 is where every
+// write to global memory lands, so the lines can never be stale.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---- numerics ----------------------------------------------------------------
 // 2^x with the MUFU.EX2 unit (PTX ex2.approx.ftz.f32); ex2(-inf) = 0.
 __device__ __forceinline__ float ex2(float x) {

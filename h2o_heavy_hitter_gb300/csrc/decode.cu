@@ -41,6 +41,7 @@ DecodeConfig decode_config(int rows, int k, int d, int num_sms, const DecodeTuni
                  ? tune.unroll
                  : (fp8 && many_rows ? 8 : 4);
   c.pdl = tune.pdl >= 0;
+  c.prefetch = tune.prefetch >= 0;
   // Measured on GB300 (decode sweeps over the workload shapes):
   //  * many rows (>= 4 per SM): one 128-thread CTA per row, one batch in flight;
   //  * fewer rows than that: 256-thread CTAs with two batches in flight per

@@ -145,6 +145,7 @@ struct DecodeShared {
   int wslot[NW];
   int is_last;
   int target;
+  int bad;         // a slot of the row held a position outside [0, t)
   float lv_score;  // ring layout: updated score of the token leaving the recent window
 };
 
@@ -176,6 +177,25 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   const int cap = max(0, min(a.seg_len, a.k - s0));
   const size_t rk = static_cast<size_t>(row) * a.k;
 
+  constexpr int EB = F8 ? 1 : 2;  // bytes per cached element
+  if constexpr (!MULTI) {
+    // This CTA's K and V slots start moving from HBM into L2 while the
+    // previous kernel in the stream drains: a bulk L2 prefetch reads nothing
+    // into the SM, so it is allowed before the dependency wait below (the
+    // previous kernel may still write one slot of the row; that write lands in
+    // L2 as well). Warp 0's lanes take 256-byte-aligned pieces of each range.
+    if (warp == 0 && cap > 0 && a.prefetch) {
+      const uint32_t bytes = static_cast<uint32_t>(cap) * D * EB;
+      const uint32_t piece = ((bytes + 31) / 32 + 255) & ~255u;
+      const uint32_t off = static_cast<uint32_t>(lane) * piece;
+      if (off < bytes) {
+        const uint32_t n = min(piece, bytes - off);
+        const size_t base = (rk + s0) * D * EB + off;
+        bulk_prefetch_l2(static_cast<const uint8_t*>(a.Kc) + base, n);
+        bulk_prefetch_l2(static_cast<const uint8_t*>(a.Vc) + base, n);
+      }
+    }
+  }
   // Everything before this wait overlaps the previous kernel's tail.
   grid_dependency_wait();  // the cache, scores and metadata are written by the previous step
   const int nsteps = MULTI ? a.steps : 1;
@@ -208,6 +228,15 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   const int32_t* meta = a.meta + static_cast<size_t>(row) * 4;
   const int count = meta[0];
   const int t = meta[1];
+  // A row holds 0 .. k tokens at distinct positions below t. Metadata that
+  // says otherwise (a cache state installed through the cache view, say) is
+  // reported and the row is left untouched: every CTA of the row reads the
+  // same values and leaves together, so no slot outside the row is written.
+  if (count < 0 || count > a.k || t < count) {
+    if (tid == 0 && seg == 0 && a.err) atomicOr(a.err, kErrBadState);
+    return;
+  }
+  if (tid == 0) sm.bad = 0;
   const int n = max(0, min(cap, count - s0));
   // ring layout: recent slots in use, heavy slots in use, the slot of position t - r (and t)
   const int nring = RING ? min(t, a.r) : 0;
@@ -237,7 +266,6 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
   float m = -INFINITY, lsum = 0.f, o[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) o[i] = 0.f;
-  constexpr int EB = F8 ? 1 : 2;  // bytes per cached element
   const uint8_t* Kg = static_cast<const uint8_t*>(a.Kc) + ((rk + s0) * D + l * 8) * EB;
   const uint8_t* Vg = static_cast<const uint8_t*>(a.Vc) + ((rk + s0) * D + l * 8) * EB;
   // A row handled by a single CTA keeps its logits in shared memory; split rows
@@ -496,6 +524,7 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
       sc = a.score[rk + i];
       ps = !RING || i < a.h ? a.pos[rk + i] : 0;
     }
+    if ((!RING || i < a.h) && (ps < 0 || ps >= t)) sm.bad = 1;  // reported below
     const float lg = solo ? solo_logits[i] : __ldcg(a.logits + rk + i);
     const float ns = sc + ex2(lg - M) * invL;
     a.score[rk + i] = ns;
@@ -543,6 +572,7 @@ __global__ void __launch_bounds__(NT) decode_kernel(const DecodeArgs a) {
         b = sm.wkey[w];
         bs = sm.wslot[w];
       }
+    if (sm.bad && a.err) atomicOr(a.err, kErrBadState);
     const bool full = count >= a.k;
     int target, evict_pos = -1;
     if constexpr (RING) {

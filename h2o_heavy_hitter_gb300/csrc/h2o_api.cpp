@@ -10,11 +10,13 @@
 #include <c10/cuda/CUDAStream.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <new>
 #include <string>
 #include <vector>
 
@@ -40,11 +42,21 @@ int env_int(const char* name) {
   return v ? std::atoi(v) : 0;
 }
 
+// Allocation-failure injection (h2o_test_fail_allocations): the next n device
+// allocations of the library throw as an exhausted allocator would.
+std::atomic<int> g_fail_allocs{0};
+
+void* device_alloc(size_t bytes, cudaStream_t s) {
+  for (int n = g_fail_allocs.load(); n > 0; n = g_fail_allocs.load())
+    if (g_fail_allocs.compare_exchange_weak(n, n - 1)) throw std::bad_alloc();
+  return c10::cuda::CUDACachingAllocator::raw_alloc_with_stream(bytes, s);
+}
+
 // One device allocation from PyTorch's caching allocator, freed on scope exit.
 struct Scratch {
   void* p = nullptr;
   explicit Scratch(size_t bytes, cudaStream_t s) {
-    if (bytes) p = c10::cuda::CUDACachingAllocator::raw_alloc_with_stream(bytes, s);
+    if (bytes) p = device_alloc(bytes, s);
   }
   ~Scratch() {
     if (p) c10::cuda::CUDACachingAllocator::raw_delete(p);
@@ -128,6 +140,8 @@ int prefill_layer(h2o_ctx* c, int layer, const void* Q, const void* K, const voi
                   const int32_t* lens, float* out) {
   if (int rc = check_layer(c, layer)) return rc;
   if (T < 0 || T > H2O_MAX_T) return fail(H2O_EINVAL, "T out of range");
+  if (c->prompt_len[layer] >= 0)
+    return fail(H2O_ESTATE, "layer already prefilled: h2o_reset it before a new prompt");
   cudaStream_t s = current_stream();
   cudaError_t e;
   if (T == 0) {
@@ -152,9 +166,9 @@ int prefill_layer(h2o_ctx* c, int layer, const void* Q, const void* K, const voi
     e = c->kv_format == H2O_KV_FP8
             ? h2o::prefill_gather_fp8(K, V, c->rows, T, c->d, c->k, c->layer_pos(layer),
                                       c->layer_K(layer), c->layer_V(layer),
-                                      c->layer_kscale(layer), c->layer_vscale(layer), s)
+                                      c->layer_kscale(layer), c->layer_vscale(layer), c->err, s)
             : h2o::prefill_gather(K, V, c->rows, T, c->d, c->k, c->layer_pos(layer),
-                                  c->layer_K(layer), c->layer_V(layer), s);
+                                  c->layer_K(layer), c->layer_V(layer), c->err, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill gather launch");
   } catch (const std::exception& ex) {
     return fail(H2O_ENOMEM, std::string("prefill scratch allocation failed: ") + ex.what());
@@ -218,7 +232,7 @@ int h2o_create_ex(int layers, int batch, int heads, int head_dim, int h, int r, 
 
   h2o::DecodeTuning tune{env_int("H2O_DECODE_THREADS"), env_int("H2O_DECODE_UNROLL"),
                          env_int("H2O_DECODE_SEGS"), env_int("H2O_DECODE_PDL"),
-                         env_int("H2O_DECODE_PIPE")};
+                         env_int("H2O_DECODE_PIPE"), env_int("H2O_DECODE_PREFETCH")};
   c->sms = sms;
   c->dcfg = h2o::decode_config(c->rows, c->k, c->d, sms, tune, kv_format == H2O_KV_FP8);
   c->mcfg = h2o::decode_multi_config(c->rows, c->k, c->d, sms, kv_format == H2O_KV_FP8);
@@ -235,7 +249,7 @@ int h2o_create_ex(int layers, int batch, int heads, int head_dim, int h, int r, 
       2 * kv_bytes + 3 * sc_bytes + 2 * qs_bytes + meta_bytes + part_bytes + cnt_bytes + 256;
   cudaStream_t s = current_stream();
   try {
-    c->base = c10::cuda::CUDACachingAllocator::raw_alloc_with_stream(total, s);
+    c->base = device_alloc(total, s);
   } catch (const std::exception& ex) {
     delete c;
     return fail(H2O_ENOMEM, std::string("cache allocation failed: ") + ex.what());
@@ -306,8 +320,11 @@ int h2o_prefill_attention(const void* Q, const void* K, const void* V, int rows,
   if (static_cast<long>(rows) * T == 0) return H2O_OK;
   if (!Q || !K || !V || !out || !score) return fail(H2O_EINVAL, "null pointer");
   if (!tma_aligned(Q, K, V, out)) return fail(H2O_EINVAL, "Q, K, V and out must be 16-byte aligned");
+  int32_t* err = nullptr;
+  cudaError_t e = h2o::attention_error_word(&err);
+  if (e != cudaSuccess) return cuda_fail(e, "error word lookup");
   try {
-    return run_attention(Q, K, V, rows, T, nullptr, 1, head_dim, out, score, nullptr,
+    return run_attention(Q, K, V, rows, T, nullptr, 1, head_dim, out, score, err,
                          current_stream());
   } catch (const std::exception& ex) {
     return fail(H2O_ENOMEM, std::string("scratch allocation failed: ") + ex.what());
@@ -329,11 +346,54 @@ int h2o_prefill_attention_noalloc(const void* Q, const void* K, const void* V, i
   float* lse = nullptr;
   cudaError_t e = h2o::noalloc_lse_scratch(&lse);
   if (e != cudaSuccess) return cuda_fail(e, "scratch address lookup");
+  int32_t* err = nullptr;
+  e = h2o::attention_error_word(&err);
+  if (e != cudaSuccess) return cuda_fail(e, "error word lookup");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  e = h2o::prefill_forward(Q, K, V, rows, T, nullptr, 1, head_dim, out, lse, nullptr, s);
+  e = h2o::prefill_forward(Q, K, V, rows, T, nullptr, 1, head_dim, out, lse, err, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefill forward launch");
-  e = h2o::prefill_colsum(Q, K, lse, rows, T, nullptr, 1, head_dim, score, nullptr, s);
+  e = h2o::prefill_colsum(Q, K, lse, rows, T, nullptr, 1, head_dim, score, err, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefill column-sum launch");
+  return H2O_OK;
+}
+
+// Reads, then clears, a device error word on `s` after the stream's work so
+// far; H2O_EDEVICE if it was set. Allocates nothing.
+static int check_error_word(int32_t* word_dev, cudaStream_t s) {
+  int32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, word_dev, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
+  if (word != 0) {
+    cudaMemsetAsync(word_dev, 0, sizeof(int32_t), s);
+    char buf[128];
+    std::snprintf(buf, sizeof(buf), "device error word 0x%x (1 = wait timeout, 2 = bad state, 4 = length out of range)", word);
+    return fail(H2O_EDEVICE, buf);
+  }
+  return H2O_OK;
+}
+
+int h2o_attention_sync_check(void* stream) {
+  int32_t* err = nullptr;
+  cudaError_t e = h2o::attention_error_word(&err);
+  if (e != cudaSuccess) return cuda_fail(e, "error word lookup");
+  return check_error_word(err, static_cast<cudaStream_t>(stream));
+}
+
+int h2o_attention_test_wait_limit(void* stream) {
+  int32_t* err = nullptr;
+  cudaError_t e = h2o::attention_error_word(&err);
+  if (e != cudaSuccess) return cuda_fail(e, "error word lookup");
+  e = h2o::wait_limit_probe(err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wait-limit probe launch");
+  return H2O_OK;
+}
+
+void h2o_forget_device_state(void) { h2o::forget_device_state(); }
+
+int h2o_test_fail_allocations(int n) {
+  if (n < 0) return fail(H2O_EINVAL, "n must be >= 0");
+  g_fail_allocs.store(n);
   return H2O_OK;
 }
 
@@ -353,6 +413,7 @@ h2o::DecodeArgs decode_args(h2o_ctx* c, int layer) {
   a.logits = c->layer_logits(layer);
   a.partial = c->layer_partial(layer);
   a.counter = c->layer_counter(layer);
+  a.err = c->err;
   a.rows = c->rows;
   a.steps = 1;
   a.k = c->k;
@@ -361,6 +422,7 @@ h2o::DecodeArgs decode_args(h2o_ctx* c, int layer) {
   a.segs = c->dcfg.segs;
   a.seg_len = c->dcfg.seg_len;
   a.qscale = h2o::kLog2e / std::sqrt(static_cast<float>(c->d));
+  a.prefetch = c->dcfg.prefetch ? 1 : 0;
   return a;
 }
 
@@ -427,6 +489,20 @@ int h2o_decode_steps(h2o_ctx* c, int layer, int steps, const void* q, const void
   return H2O_OK;
 }
 
+int h2o_reset(h2o_ctx* c, int layer) {
+  if (!c) return fail(H2O_EINVAL, "null context");
+  if (layer < -1 || layer >= c->layers) return fail(H2O_EINVAL, "layer out of range");
+  const int l0 = layer < 0 ? 0 : layer, l1 = layer < 0 ? c->layers : layer + 1;
+  cudaStream_t s = current_stream();
+  for (int l = l0; l < l1; ++l) {
+    cudaError_t e = h2o::cache_reset(c->rows, c->k, c->layer_score(l), c->layer_pos(l),
+                                     c->layer_meta(l), s);
+    if (e != cudaSuccess) return cuda_fail(e, "cache reset");
+    c->prompt_len[l] = -1;
+  }
+  return H2O_OK;
+}
+
 int h2o_cache_positions(h2o_ctx* c, int layer, int32_t* host_pos) {
   if (int rc = check_layer(c, layer)) return rc;
   if (!host_pos) return fail(H2O_EINVAL, "null host buffer");
@@ -484,18 +560,7 @@ int h2o_test_wait_limit(h2o_ctx* c) {
 
 int h2o_sync_check(h2o_ctx* c) {
   if (!c) return fail(H2O_EINVAL, "null context");
-  cudaStream_t s = current_stream();
-  int32_t word = 0;
-  cudaError_t e = cudaMemcpyAsync(&word, c->err, sizeof(word), cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
-  if (word != 0) {
-    cudaMemsetAsync(c->err, 0, sizeof(int32_t), s);
-    char buf[128];
-    std::snprintf(buf, sizeof(buf), "device error word 0x%x (1 = wait timeout, 2 = bad state, 4 = length out of range)", word);
-    return fail(H2O_EDEVICE, buf);
-  }
-  return H2O_OK;
+  return check_error_word(c->err, current_stream());
 }
 
 }  // extern "C"

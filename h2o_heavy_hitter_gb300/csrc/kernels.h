@@ -29,6 +29,7 @@ struct DecodeArgs {
   const void* v_new;  // bf16 [steps][rows][d]
   float* out;         // [steps][rows][d]
   int32_t* evicted;   // [steps][rows] evicted position (-1 none) of each step, or null
+  int32_t* err;       // device error word: kErrBadState when a row's cache state is inconsistent
   int rows;           // rows of the layer
   int steps;          // steps per launch (1 except for the multi-step launcher)
   int k;              // slots per row (h + r)
@@ -37,6 +38,7 @@ struct DecodeArgs {
   int segs;           // CTAs per row
   int seg_len;        // slots per segment (the last may be shorter)
   float qscale;       // log2(e) / sqrt(d)
+  int prefetch;       // pull the CTA's K/V slots into L2 before the dependency wait
 };
 
 // Launch shape of the decode kernel. Zero / out-of-range values pick defaults.
@@ -46,11 +48,13 @@ struct DecodeTuning {
   int segs;     // CTAs per row; 0 = automatic
   int pdl;      // < 0: launch without programmatic dependent launch
   int pipe;     // > 0: two batches per group in flight; < 0: one; 0: automatic
+  int prefetch; // < 0: no L2 prefetch before the dependency wait
 };
 
 struct DecodeConfig {
   bool pdl;     // programmatic dependent launch (overlaps the previous kernel's tail)
   bool pipe;    // two batches per group in flight
+  bool prefetch;  // K/V slots pulled into L2 before the dependency wait
   int threads, unroll;
   int segs;     // CTAs per row
   int seg_len;  // slots per segment
@@ -99,6 +103,12 @@ cudaError_t prefill_colsum(const void* Q, const void* K, const float* lse2, int 
 // h2o_prefill_attention_noalloc (H2O_NOALLOC_MAX_LSE floats). Looked up once
 // per device, with that device current, and cached.
 cudaError_t noalloc_lse_scratch(float** out);
+// Device address of the library-level error word (int32) that the cache-free
+// prefill entry points pass to their kernels; looked up like the array above.
+cudaError_t attention_error_word(int32_t** out);
+// Drops every cached per-device address and kernel attribute, so that the
+// next call looks them up again (after a device reset).
+void forget_device_state();
 
 // Top-h plus recent selection of every row into the cache's pos/score/meta
 // (colsum rows T floats apart; per-row lengths as for prefill_forward; a
@@ -109,15 +119,17 @@ cudaError_t noalloc_lse_scratch(float** out);
 cudaError_t prefill_select(const float* colsum, int rows, int T, const int32_t* lens, int heads,
                            int h, int r, bool ring, float* score, int32_t* pos, int32_t* meta,
                            int32_t* err, cudaStream_t stream);
-// Copies the selected prompt K/V rows into the cache slots.
+// Copies the selected prompt K/V rows into the cache slots (a position outside
+// [0, T) is skipped and sets kErrBadState in *err).
 cudaError_t prefill_gather(const void* K, const void* V, int rows, int T, int d, int k,
-                           const int32_t* pos, void* Kc, void* Vc, cudaStream_t stream);
+                           const int32_t* pos, void* Kc, void* Vc, int32_t* err,
+                           cudaStream_t stream);
 // Resets rows to an empty cache (pos -1, score 0, meta {0, 0, -1, 0}).
 // E4M3 cache: the kept tokens quantised into their slots, codes plus one fp32
 // scale per slot for K and for V.
 cudaError_t prefill_gather_fp8(const void* K, const void* V, int rows, int T, int d, int k,
                                const int32_t* pos, void* Kc, void* Vc, float* kscale,
-                               float* vscale, cudaStream_t stream);
+                               float* vscale, int32_t* err, cudaStream_t stream);
 cudaError_t cache_reset(int rows, int k, float* score, int32_t* pos, int32_t* meta,
                         cudaStream_t stream);
 // One kernel whose bounded wait is never satisfied: it gives up after the

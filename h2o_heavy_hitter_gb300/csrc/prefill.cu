@@ -858,6 +858,33 @@ int rows_per_l2_block(int T, int D, int tensors) {
   return rb < 1 ? 1 : rb;
 }
 
+// Per-device state of this file (kernel attributes, looked-up symbol
+// addresses) is kept for devices 0 .. kMaxDevices - 1 under one mutex.
+// forget_device_state() starts a new epoch, which invalidates all of it.
+constexpr int kMaxDevices = 64;
+std::mutex g_device_state_mutex;
+int g_device_state_epoch = 1;
+
+// Lets `kernel` use `bytes` of dynamic shared memory on the current device.
+// The attribute is per device, so it is set once per device and epoch;
+// opted_in[dev] records the epoch in which it was set (guarded by the mutex,
+// so concurrent first calls are safe).
+template <typename Kernel>
+cudaError_t raise_smem_limit(Kernel kernel, size_t bytes, int (&opted_in)[kMaxDevices]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_device_state_mutex);
+  if (opted_in[dev] != g_device_state_epoch) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(bytes));
+    if (e != cudaSuccess) return e;
+    opted_in[dev] = g_device_state_epoch;
+  }
+  return cudaSuccess;
+}
+
 // SM count of the current device (one persistent CTA per SM).
 int num_sms() {
   int dev = 0, n = 0;
@@ -909,13 +936,8 @@ cudaError_t forward_t(const void* Q, const void* K, const void* V, int rows, int
   if ((e = make_map(&mk, K, rows, T, D)) != cudaSuccess) return e;
   if ((e = make_map(&mv, V, rows, T, D)) != cudaSuccess) return e;
   if ((e = make_store_map(&mo, O, rows, T, D)) != cudaSuccess) return e;
-  static bool attr = false;
-  if (!attr) {
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(FwdCfg<D>::SMEM));
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static int opted_in[kMaxDevices] = {};
+  if ((e = raise_smem_limit(attn_fwd_kernel<D>, FwdCfg<D>::SMEM, opted_in)) != cudaSuccess) return e;
   const int nqt = (T + BM - 1) / BM, nqb = (nqt + 1) / 2;
   FwdParams p{lse2, lens, heads, rows, T, lse_stride(T), nqt, nqb, rows * nqb,
               rows_per_l2_block(T, D, 2), kLog2e / sqrtf(float(D)), err};
@@ -932,13 +954,9 @@ cudaError_t colsum_t(const void* Q, const void* K, const float* lse2, int rows, 
   cudaError_t e;
   if ((e = make_map(&mq, Q, rows, T, D)) != cudaSuccess) return e;
   if ((e = make_map(&mk, K, rows, T, D)) != cudaSuccess) return e;
-  static bool attr = false;
-  if (!attr) {
-    e = cudaFuncSetAttribute(attn_colsum_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(ColCfg<D>::SMEM));
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static int opted_in[kMaxDevices] = {};
+  if ((e = raise_smem_limit(attn_colsum_kernel<D>, ColCfg<D>::SMEM, opted_in)) != cudaSuccess)
+    return e;
   const int nqt = (T + BM - 1) / BM;
   ColParams p{lse2, colsum, lens, heads, rows, T, lse_stride(T), nqt, rows * nqt,
               rows_per_l2_block(T, D, 1), kLog2e / sqrtf(float(D)), err};
@@ -967,31 +985,50 @@ cudaError_t prefill_colsum(const void* Q, const void* K, const float* lse2, int 
 
 // ------------------------------------------------------------------ allocation-free scratch
 // Per-row log-sum-exp for h2o_prefill_attention_noalloc lives in this fixed
-// file-scope device array instead of an allocation. Host code must not pass
-// the symbol itself to a kernel (on the host it is only a stand-in); its
-// device address is looked up per device below.
+// file-scope device array instead of an allocation, and the cache-free entry
+// points report bounded waits that gave up through the error word next to it.
+// Host code must not pass either symbol itself to a kernel (on the host it is
+// only a stand-in); their device addresses are looked up per device below.
 static __device__ __align__(256) float g_noalloc_lse[H2O_NOALLOC_MAX_LSE];
+static __device__ __align__(16) int32_t g_attention_err[4];
 
 namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mutex;
 float* g_noalloc_ptr[kMaxDevices] = {};
-}  // namespace
+int32_t* g_attention_err_ptr[kMaxDevices] = {};
 
-cudaError_t noalloc_lse_scratch(float** out) {
+// Device address of `symbol` on the current device, looked up once per device
+// with that device current and cached in slot[dev].
+template <typename T, typename Sym>
+cudaError_t device_symbol(T* (&slot)[kMaxDevices], const Sym& symbol, T** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  std::lock_guard<std::mutex> lock(g_device_state_mutex);
+  if (slot[dev] == nullptr) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_lse);
+    e = cudaGetSymbolAddress(&p, symbol);
     if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = static_cast<float*>(p);
+    slot[dev] = static_cast<T*>(p);
   }
-  *out = g_noalloc_ptr[dev];
+  *out = slot[dev];
   return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t noalloc_lse_scratch(float** out) { return device_symbol(g_noalloc_ptr, g_noalloc_lse, out); }
+
+cudaError_t attention_error_word(int32_t** out) {
+  return device_symbol(g_attention_err_ptr, g_attention_err, out);
+}
+
+void forget_device_state() {
+  std::lock_guard<std::mutex> lock(g_device_state_mutex);
+  for (int i = 0; i < kMaxDevices; ++i) {
+    g_noalloc_ptr[i] = nullptr;
+    g_attention_err_ptr[i] = nullptr;
+  }
+  ++g_device_state_epoch;
 }
 
 }  // namespace h2o

@@ -190,7 +190,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __rest
                                                     const __nv_bfloat16* __restrict__ V, int T,
                                                     int k, const int32_t* __restrict__ pos,
                                                     __nv_bfloat16* __restrict__ Kc,
-                                                    __nv_bfloat16* __restrict__ Vc) {
+                                                    __nv_bfloat16* __restrict__ Vc,
+                                                    int32_t* __restrict__ err) {
   constexpr int CH = D / 8;  // 16-byte chunks per row
   const int row = blockIdx.x;
   const int slot = blockIdx.y * 8 + (threadIdx.x >> 5);
@@ -198,6 +199,10 @@ __global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __rest
   if (slot >= k) return;
   const int p = pos[static_cast<size_t>(row) * k + slot];
   if (p < 0) return;
+  if (p >= T) {  // never written by the selection; reported, nothing is read
+    if (lane == 0 && err) atomicOr(err, kErrBadState);
+    return;
+  }
   const size_t src = (static_cast<size_t>(row) * T + p) * D;
   const size_t dst = (static_cast<size_t>(row) * k + slot) * D;
   for (int c = lane; c < 2 * CH; c += 32) {
@@ -217,7 +222,8 @@ __global__ void __launch_bounds__(256) gather_fp8_kernel(const __nv_bfloat16* __
                                                         uint8_t* __restrict__ Kc,
                                                         uint8_t* __restrict__ Vc,
                                                         float* __restrict__ kscale,
-                                                        float* __restrict__ vscale) {
+                                                        float* __restrict__ vscale,
+                                                        int32_t* __restrict__ err) {
   constexpr int EPL = D / 32;  // values per lane: 4 (d = 128) or 2 (d = 64)
   const int row = blockIdx.x;
   const int slot = blockIdx.y * 8 + (threadIdx.x >> 5);
@@ -225,6 +231,10 @@ __global__ void __launch_bounds__(256) gather_fp8_kernel(const __nv_bfloat16* __
   if (slot >= k) return;  // whole warps leave together: the shuffles below see full warps
   const int p = pos[static_cast<size_t>(row) * k + slot];
   if (p < 0) return;
+  if (p >= T) {  // never written by the selection; reported, nothing is read
+    if (lane == 0 && err) atomicOr(err, kErrBadState);
+    return;
+  }
   const size_t src = (static_cast<size_t>(row) * T + p) * D + lane * EPL;
   const size_t dst = (static_cast<size_t>(row) * k + slot) * D + lane * EPL;
 #pragma unroll
@@ -288,7 +298,8 @@ cudaError_t prefill_select(const float* colsum, int rows, int T, const int32_t* 
 }
 
 cudaError_t prefill_gather(const void* K, const void* V, int rows, int T, int d, int k,
-                           const int32_t* pos, void* Kc, void* Vc, cudaStream_t stream) {
+                           const int32_t* pos, void* Kc, void* Vc, int32_t* err,
+                           cudaStream_t stream) {
   if (rows == 0 || T == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>((k + 7) / 8));
   auto kk = static_cast<const __nv_bfloat16*>(K);
@@ -296,15 +307,15 @@ cudaError_t prefill_gather(const void* K, const void* V, int rows, int T, int d,
   auto kc = static_cast<__nv_bfloat16*>(Kc);
   auto vc = static_cast<__nv_bfloat16*>(Vc);
   if (d == 128)
-    gather_kernel<128><<<grid, 256, 0, stream>>>(kk, vv, T, k, pos, kc, vc);
+    gather_kernel<128><<<grid, 256, 0, stream>>>(kk, vv, T, k, pos, kc, vc, err);
   else
-    gather_kernel<64><<<grid, 256, 0, stream>>>(kk, vv, T, k, pos, kc, vc);
+    gather_kernel<64><<<grid, 256, 0, stream>>>(kk, vv, T, k, pos, kc, vc, err);
   return cudaGetLastError();
 }
 
 cudaError_t prefill_gather_fp8(const void* K, const void* V, int rows, int T, int d, int k,
                                const int32_t* pos, void* Kc, void* Vc, float* kscale,
-                               float* vscale, cudaStream_t stream) {
+                               float* vscale, int32_t* err, cudaStream_t stream) {
   if (rows == 0 || T == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>((k + 7) / 8));
   auto kk = static_cast<const __nv_bfloat16*>(K);
@@ -312,9 +323,10 @@ cudaError_t prefill_gather_fp8(const void* K, const void* V, int rows, int T, in
   auto kc = static_cast<uint8_t*>(Kc);
   auto vc = static_cast<uint8_t*>(Vc);
   if (d == 128)
-    gather_fp8_kernel<128><<<grid, 256, 0, stream>>>(kk, vv, T, k, pos, kc, vc, kscale, vscale);
+    gather_fp8_kernel<128><<<grid, 256, 0, stream>>>(kk, vv, T, k, pos, kc, vc, kscale, vscale,
+                                                     err);
   else
-    gather_fp8_kernel<64><<<grid, 256, 0, stream>>>(kk, vv, T, k, pos, kc, vc, kscale, vscale);
+    gather_fp8_kernel<64><<<grid, 256, 0, stream>>>(kk, vv, T, k, pos, kc, vc, kscale, vscale, err);
   return cudaGetLastError();
 }
 

@@ -46,7 +46,8 @@ extern "C" {
 
 #define H2O_OK 0
 #define H2O_EINVAL (-1)  /* bad argument (null pointer, size out of range, layer out of range) */
-#define H2O_ESTATE (-2)  /* call not valid in the current state (decode before prefill) */
+#define H2O_ESTATE (-2)  /* call not valid in the current state (decode before prefill, or a
+                            second prefill of a layer without h2o_reset) */
 #define H2O_ENOMEM (-3)  /* device allocation failed */
 #define H2O_ECUDA (-4)   /* a CUDA runtime call or kernel launch failed */
 #define H2O_EDEVICE (-5) /* a kernel reported an error through the device error word */
@@ -124,16 +125,33 @@ void h2o_destroy(h2o_ctx* ctx);
  * the cache then holds the r most recent tokens T-r .. T-1 plus the h other
  * tokens with the largest (score, position) keys, or every token if T <= h + r.
  * Ties in score keep the later position. Retained tokens keep their column
- * sums as accumulated scores. The layer's previous cache content is replaced.
+ * sums as accumulated scores.
+ *
+ * State: a layer takes one prompt ([H2O] A, Pseudocode: the prompt's heavy
+ * hitters are selected once, then generation proceeds step by step). The
+ * layer must be empty, as h2o_create or h2o_reset leaves it; a second prefill
+ * without h2o_reset returns H2O_ESTATE and changes nothing. After a prefill
+ * that fails the layer still counts as empty: decode returns H2O_ESTATE and
+ * the next prefill is accepted.
  *
  * Q, K, V: device bf16 [batch, heads, T, d]; out: device fp32 [batch, heads, T, d].
  * 0 <= T <= H2O_MAX_T; with T = 0 the pointers may be NULL and the layer is
  * reset to an empty cache. Scratch (per-row log-sum-exp and column sums,
  * 8 bytes per prompt token) comes from PyTorch's caching allocator on the
- * current stream. Errors: H2O_EINVAL, H2O_ENOMEM, H2O_ECUDA.
+ * current stream. Errors: H2O_EINVAL, H2O_ESTATE (layer not empty), H2O_ENOMEM,
+ * H2O_ECUDA.
  */
 int h2o_prefill(h2o_ctx* ctx, int layer, const void* Q, const void* K, const void* V, int T,
                 float* out);
+
+/*
+ * h2o_reset - return one layer (layer >= 0) or every layer (layer = -1) to the
+ * empty state h2o_create leaves: no token cached (positions -1, scores 0, fill
+ * count and next position 0), ready for a new prompt (h2o_prefill). Enqueues
+ * one small kernel per layer on the current stream; allocates nothing.
+ * Errors: H2O_EINVAL (null context, layer out of range), H2O_ECUDA.
+ */
+int h2o_reset(h2o_ctx* ctx, int layer);
 
 /*
  * h2o_prefill_ragged - h2o_prefill of a batch whose prompts differ in length
@@ -157,8 +175,9 @@ int h2o_prefill(h2o_ctx* ctx, int layer, const void* Q, const void* K, const voi
  * value is not 0. out: device fp32 [batch, heads, T_max, d]; rows t >= T_b
  * hold no result (the call may write them). Scratch as for h2o_prefill, sized
  * by T_max. With T_max = 0 the pointers may be NULL and every row is reset to
- * an empty cache. Errors: H2O_EINVAL (also for lens NULL with T_max > 0),
- * H2O_ENOMEM, H2O_ECUDA.
+ * an empty cache. The layer must be empty, as for h2o_prefill. Errors:
+ * H2O_EINVAL (also for lens NULL with T_max > 0), H2O_ESTATE, H2O_ENOMEM,
+ * H2O_ECUDA.
  */
 int h2o_prefill_ragged(h2o_ctx* ctx, int layer, const void* Q, const void* K, const void* V,
                        int T_max, const int32_t* lens, float* out);
@@ -181,6 +200,13 @@ int h2o_prefill_ragged(h2o_ctx* ctx, int layer, const void* Q, const void* K, co
  * live in device memory and are advanced by the kernel, so the call can be
  * captured in a CUDA graph and replayed. Errors: H2O_EINVAL, H2O_ESTATE (layer
  * never prefilled), H2O_ECUDA.
+ *
+ * The kernel checks each row's state before it touches the row: a fill count
+ * outside [0, k] or above the next position t, or an occupied slot whose
+ * position is outside [0, t) (a state installed through h2o_cache_view that
+ * no call of this library produces), sets bit 2 (bad state) of the device
+ * error word, and a row with inconsistent counts is left unchanged.
+ * h2o_sync_check then reports H2O_EDEVICE.
  */
 int h2o_decode_step(h2o_ctx* ctx, int layer, const void* q, const void* k_new, const void* v_new,
                     float* out);
@@ -214,6 +240,8 @@ int h2o_decode_steps(h2o_ctx* ctx, int layer, int steps, const void* q, const vo
  * Q, K, V: device bf16 [rows, T, d]; out: device fp32 [rows, T, d];
  * score: device fp32 [rows, T]. Scratch (per-row log-sum-exp, 4 bytes per
  * token) comes from PyTorch's caching allocator on the current stream.
+ * A bounded device wait that gives up is reported through the library's own
+ * error word (h2o_attention_sync_check), since no context is involved.
  * Errors: H2O_EINVAL, H2O_ENOMEM, H2O_ECUDA.
  */
 int h2o_prefill_attention(const void* Q, const void* K, const void* V, int rows, int T,
@@ -246,6 +274,19 @@ int h2o_prefill_attention(const void* Q, const void* K, const void* V, int rows,
  * ordered and safe. Nothing in the array needs to start at zero: every entry a
  * call reads was written earlier by the same call.
  *
+ * Where the array lives: CUDA loads a library's device code, and with it this
+ * array, into a device on first use (lazy module loading is the default), so
+ * the first call on each device may itself need 4 MiB of free device memory.
+ * Make one small call on each device at start-up, before an arena reserves the
+ * rest of the memory (and before any stream capture). The looked-up address
+ * belongs to the device's context: after cudaDeviceReset on that device, call
+ * h2o_forget_device_state() before the next call, which then looks it up
+ * again.
+ *
+ * Errors inside the kernels: a bounded device wait that gives up sets the
+ * library's error word, which h2o_attention_sync_check(stream) reports (the
+ * word is also a fixed device variable, not an allocation).
+ *
  * Q, K, V: device bf16 [rows, T, d]; out: device fp32 [rows, T, d];
  * score: device fp32 [rows, T]. Limit: rows * (T rounded up to a multiple of
  * 128) <= H2O_NOALLOC_MAX_LSE; larger calls are rejected with H2O_EINVAL and
@@ -254,6 +295,45 @@ int h2o_prefill_attention(const void* Q, const void* K, const void* V, int rows,
 #define H2O_NOALLOC_MAX_LSE (1 << 20)
 int h2o_prefill_attention_noalloc(const void* Q, const void* K, const void* V, int rows, int T,
                                   int head_dim, float* out, float* score, void* stream);
+
+/*
+ * h2o_attention_sync_check - synchronise `stream` (a cudaStream_t; NULL is the
+ * legacy default stream) and report, then clear, the library-level device
+ * error word of the current device that the cache-free entry points
+ * (h2o_prefill_attention, h2o_prefill_attention_noalloc) write: bit 1 when
+ * one of their bounded waits gave up (their outputs are then incomplete).
+ * Allocates nothing. The word is shared by every such call on the device.
+ * Errors: H2O_ECUDA, H2O_EDEVICE.
+ */
+int h2o_attention_sync_check(void* stream);
+
+/*
+ * h2o_attention_test_wait_limit - the failure path of the cache-free entry
+ * points on demand: enqueues on `stream` one kernel whose bounded wait is
+ * never satisfied; after the wait limit (2 s) it sets bit 1 of the
+ * library-level error word and returns. The next h2o_attention_sync_check
+ * reports H2O_EDEVICE. Errors: H2O_ECUDA.
+ */
+int h2o_attention_test_wait_limit(void* stream);
+
+/*
+ * h2o_forget_device_state - drop the per-device state the library caches (the
+ * device addresses of its fixed arrays and its kernels' shared-memory
+ * opt-ins), so that the next call on each device sets it up again. Needed
+ * only after cudaDeviceReset (which discards a device's context, and with it
+ * the library's loaded code and arrays); call it with no work of the library
+ * in flight. Contexts made by h2o_create do not survive a device reset.
+ */
+void h2o_forget_device_state(void);
+
+/*
+ * h2o_test_fail_allocations - fault injection on the host: the next n device
+ * allocations the library makes (a cache in h2o_create, prefill scratch) fail
+ * as an exhausted allocator would, and the calls return H2O_ENOMEM with the
+ * state unchanged (no context is created; a layer whose prefill failed stays
+ * empty). n = 0 ends it. No GPU work is involved. Errors: H2O_EINVAL (n < 0).
+ */
+int h2o_test_fail_allocations(int n);
 
 /*
  * h2o_cache_positions - copy the positions held by every slot of one layer to

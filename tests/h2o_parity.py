@@ -40,9 +40,12 @@ from parity_rows import MAX_ABS, MEAN_ABS, SCORE_RTOL  # noqa: F401  (re-exporte
 from workloads import Workload, bf16_bits_to_f64, head_direction, layer_tokens, row_tokens
 
 # Default bound on near-ties: at most this fraction of all eviction and prefill
-# boundary checks may fall below the near-tie margin (the observed rates are
-# far lower; a larger share would mean the excused decisions carry weight).
+# boundary checks may fall below the near-tie margin, plus NEAR_TIE_SLACK for
+# runs too small for a rate (the observed rates are 0.003 % to 0.04 % on the
+# full-size workloads; a larger share would mean the excused decisions carry
+# weight).
 NEAR_TIE_RATE_MAX = 0.01
+NEAR_TIE_SLACK = 2
 
 
 def _workers(n_jobs: int) -> int:
@@ -88,12 +91,16 @@ class Report:
     def near_tie_rate(self) -> float:
         return self.near_ties / max(1, self.evict_checks + self.prefill_checks)
 
+    def near_ties_bounded(self, near_tie_rate_max: float = NEAR_TIE_RATE_MAX) -> bool:
+        checks = self.evict_checks + self.prefill_checks
+        return self.near_ties <= max(NEAR_TIE_SLACK, near_tie_rate_max * checks)
+
     def ok(self, near_tie_rate_max: float = NEAR_TIE_RATE_MAX) -> bool:
         return (not self.mismatches and not self.code_mismatches and self.prefill_max_abs <= MAX_ABS
                 and self.prefill_mean_abs <= MEAN_ABS and self.decode_max_abs <= MAX_ABS
                 and self.decode_mean_abs <= MEAN_ABS and self.score_max_rel <= SCORE_RTOL
                 and self.near_tie_mismatches <= self.near_ties
-                and self.near_tie_rate() <= near_tie_rate_max)
+                and self.near_ties_bounded(near_tie_rate_max))
 
     def summary(self, label: str) -> str:
         return (f"[{label}] rows={self.rows} steps={self.steps} evict_checks={self.evict_checks} "
@@ -115,7 +122,7 @@ def assert_report(rep: Report, label: str, near_tie_rate_max: float = NEAR_TIE_R
     assert rep.decode_max_abs <= MAX_ABS and rep.decode_mean_abs <= MEAN_ABS
     assert rep.score_max_rel <= SCORE_RTOL, rep.score_max_rel
     assert rep.near_tie_mismatches <= rep.near_ties
-    assert rep.near_tie_rate() <= near_tie_rate_max, (rep.near_ties, rep.near_tie_rate())
+    assert rep.near_ties_bounded(near_tie_rate_max), (rep.near_ties, rep.near_tie_rate())
     assert rep.ok(near_tie_rate_max)
 
 

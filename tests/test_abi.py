@@ -93,3 +93,17 @@ def test_new_entry_points_check_arguments_without_gpu(lib):
     assert lib.h2o_create_ex(1, 1, 1, 64, 4, 4, 1 | ring, ctypes.byref(out)) == -1  # FP8 + ring
     assert lib.h2o_create_ex(1, 1, 1, 64, 4, 4, 7, ctypes.byref(out)) == -1  # unknown format
     assert out.value is None
+
+
+def test_state_and_fault_entry_points_check_arguments_without_gpu(lib):
+    """h2o_reset, the allocation-failure hook and the device-state reset run
+    their argument checks (or touch only host state) without any CUDA call."""
+    P, I = ctypes.c_void_p, ctypes.c_int
+    lib.h2o_last_error.restype = ctypes.c_char_p
+    lib.h2o_reset.argtypes = [P, I]
+    assert lib.h2o_reset(None, 0) == -1 and b"null context" in lib.h2o_last_error()
+    lib.h2o_test_fail_allocations.argtypes = [I]
+    assert lib.h2o_test_fail_allocations(-1) == -1
+    assert lib.h2o_test_fail_allocations(0) == 0
+    lib.h2o_forget_device_state.restype = None
+    lib.h2o_forget_device_state()

@@ -5,8 +5,9 @@ the library instead of an allocation).
 It is called through the C ABI twice in a row, on different shapes and data,
 and each time compared with h2o_prefill_attention (which allocates its scratch)
 using the same tolerances as the other prefill parity tests. A request larger
-than the fixed scratch must be refused with H2O_EINVAL. This file is named so
-that pytest collects it last; it also passes when run on its own.
+than the fixed scratch must be refused with H2O_EINVAL, and the call must run
+on the stream it is given, not on the caller's current stream. This file is
+named so that pytest collects it last; it also passes when run on its own.
 """
 import ctypes
 
@@ -80,3 +81,30 @@ def test_noalloc_refuses_sizes_beyond_its_scratch():
     rc = lib.h2o_prefill_attention_noalloc(None, None, None, rows, T, 128, None, None, None)
     assert rc == -1
     assert b"exceeds the fixed scratch" in lib.h2o_last_error()
+
+
+def test_noalloc_runs_on_the_stream_it_is_given():
+    """With the current stream busy (a long spin kernel queued on it), a call
+    given another stream must still finish on that stream: copies of its
+    outputs queued behind it on the same stream see finished results. Had the
+    kernels gone to the current stream, the copies would run first and hold
+    the NaN fill."""
+    h2o, lib = _lib()
+    Q, K, V = _inputs(292, 1, 2, 128, 257)
+    ref = h2o.h2o_prefill_attention(Q, K, V)
+    rows, T, d = Q.shape
+    out = torch.full((rows, T, d), float("nan"), dtype=torch.float32, device=Q.device)
+    score = torch.full((rows, T), float("nan"), dtype=torch.float32, device=Q.device)
+    out_c, score_c = torch.empty_like(out), torch.empty_like(score)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    torch.cuda._sleep(200_000_000)  # about 0.1 s of work on the current stream
+    rc = lib.h2o_prefill_attention_noalloc(Q.data_ptr(), K.data_ptr(), V.data_ptr(), rows, T, d,
+                                           out.data_ptr(), score.data_ptr(), side.cuda_stream)
+    assert rc == 0, lib.h2o_last_error()
+    with torch.cuda.stream(side):
+        out_c.copy_(out)
+        score_c.copy_(score)
+    torch.cuda.synchronize()
+    _compare((out_c, score_c), ref)
+    h2o.h2o_attention_sync_check(side)  # no device error reported by the kernels
