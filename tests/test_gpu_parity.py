@@ -186,6 +186,7 @@ def test_long_stream_soak_constant_memory():
     """Decode 16x the budget past the prompt: evictions keep matching the oracle,
     scores stay finite and the device memory in use does not grow."""
     w = Workload(280, "soak", 1, 1, 4, 64, 96, 2048, 64, 64, 0.8)
+    gc.collect()  # tensors left over by earlier tests must not be freed during the count
     torch.cuda.synchronize()
     before = torch.cuda.memory_allocated()
     rep = run_parity(w, set_check_every=256)
