@@ -30,7 +30,7 @@ KernelFn pick(const DecodeConfig& c, int d, bool f8) { return f8 ? pick_f<true>(
 }  // namespace
 
 DecodeConfig decode_config(int rows, int k, int d, int num_sms, const DecodeTuning& tune,
-                           bool fp8) {
+                           bool fp8, long long l2_bytes) {
   DecodeConfig c{};
   const bool few_rows = rows < num_sms;
   const bool many_rows = rows >= 4 * num_sms;
@@ -41,7 +41,13 @@ DecodeConfig decode_config(int rows, int k, int d, int num_sms, const DecodeTuni
                  ? tune.unroll
                  : (fp8 && many_rows ? 8 : 4);
   c.pdl = tune.pdl >= 0;
-  c.prefetch = tune.prefetch >= 0;
+  // The L2 prefetch before the dependency wait pays only when a launch's K/V
+  // fits comfortably in L2: a larger sweep evicts the prefetched lines before
+  // it reads them, and HBM moves them twice (measured: 128 rows x 4096 slots,
+  // 275 MB, 49 -> 66 us per step with the prefetch; 8192 rows x 410 slots,
+  // 262 -> 303 us).
+  const long long kv_bytes = 2LL * rows * k * d * (fp8 ? 1 : 2);
+  c.prefetch = tune.prefetch > 0 || (tune.prefetch == 0 && 5 * kv_bytes <= 3 * l2_bytes);
   // Measured on GB300 (decode sweeps over the workload shapes):
   //  * many rows (>= 4 per SM): one 128-thread CTA per row, one batch in flight;
   //  * fewer rows than that: 256-thread CTAs with two batches in flight per

@@ -223,8 +223,9 @@ int h2o_create_ex(int layers, int batch, int heads, int head_dim, int h, int r, 
     delete c;
     return fail(H2O_ECUDA, std::string("no CUDA device: ") + ex.what());
   }
-  int sms = 0;
+  int sms = 0, l2 = 0;
   cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, c->device);
   if (e != cudaSuccess) {
     delete c;
     return cuda_fail(e, "cudaDeviceGetAttribute");
@@ -234,7 +235,7 @@ int h2o_create_ex(int layers, int batch, int heads, int head_dim, int h, int r, 
                          env_int("H2O_DECODE_SEGS"), env_int("H2O_DECODE_PDL"),
                          env_int("H2O_DECODE_PIPE"), env_int("H2O_DECODE_PREFETCH")};
   c->sms = sms;
-  c->dcfg = h2o::decode_config(c->rows, c->k, c->d, sms, tune, kv_format == H2O_KV_FP8);
+  c->dcfg = h2o::decode_config(c->rows, c->k, c->d, sms, tune, kv_format == H2O_KV_FP8, l2);
   c->mcfg = h2o::decode_multi_config(c->rows, c->k, c->d, sms, kv_format == H2O_KV_FP8);
 
   const size_t L = layers, R = c->rows, K = c->k, D = head_dim;

@@ -48,7 +48,7 @@ struct DecodeTuning {
   int segs;     // CTAs per row; 0 = automatic
   int pdl;      // < 0: launch without programmatic dependent launch
   int pipe;     // > 0: two batches per group in flight; < 0: one; 0: automatic
-  int prefetch; // < 0: no L2 prefetch before the dependency wait
+  int prefetch; // > 0: L2 prefetch before the dependency wait; < 0: none; 0: automatic
 };
 
 struct DecodeConfig {
@@ -61,9 +61,10 @@ struct DecodeConfig {
   size_t smem;  // dynamic shared memory per CTA (logits of a single-CTA row)
 };
 
-// Picks the launch shape for (rows, k, d) on a device with `num_sms` SMs.
+// Picks the launch shape for (rows, k, d) on a device with `num_sms` SMs and
+// an L2 of `l2_bytes`.
 DecodeConfig decode_config(int rows, int k, int d, int num_sms, const DecodeTuning& tune,
-                           bool fp8);
+                           bool fp8, long long l2_bytes);
 cudaError_t decode_launch(const DecodeArgs& a, const DecodeConfig& cfg, int rows, int d,
                           cudaStream_t stream);
 // The same step for a cache in the ring layout (bf16, r >= 1): heavy slots
