@@ -40,7 +40,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from workloads import (WORKLOADS, decode_bytes_per_row_step, head_direction,  # noqa: E402
-                       prefill_flops_per_row, row_tokens)
+                       prefill_bytes_per_row, prefill_flops_per_row, row_tokens)
 
 METRIC = "H2O decode tokens/s/GPU at 20% KV budget; achieved HBM GB/s vs peak"
 UNIT = "tokens/s"
@@ -592,6 +592,12 @@ def run_ours(args, w):
     hbm = float(peaks["hbm_gbs"])
     pflops = prefill_flops_per_row(T, d) * rows * L
     pre_tflops = pflops / (prefill_ms * 1e-3) / 1e12
+    # The prefill's ceiling is the lower of the tensor peak and what HBM can
+    # feed at its arithmetic intensity (short prompts fall under the ridge).
+    pbytes = prefill_bytes_per_row(T, d, w.k, args.kv) * rows * L
+    tensor_peak = float(peaks["bf16_tflops"])
+    hbm_ceiling = pflops / pbytes * float(peaks["hbm_gbs"]) / 1e3
+    pre_ceiling = min(tensor_peak, hbm_ceiling)
     tokens = B * S * args.steps * ws
     value = tokens / (elapsed_ms * 1e-3)
     roof = {"kernel": "h2o decode_kernel", "bound": "hbm", "peak": hbm, "unit": "GB/s",
@@ -627,7 +633,11 @@ def run_ours(args, w):
         "phases": {"prefill_ms": prefill_ms, "decode_ms": decode_ms,
                    "prefill_tokens_per_s": B * T * L / (prefill_ms * 1e-3),
                    "prefill_tflops": pre_tflops,
-                   "prefill_frac_bf16": pre_tflops / float(peaks["bf16_tflops"]),
+                   "prefill_frac_bf16": pre_tflops / tensor_peak,
+                   "prefill_bytes": pbytes,
+                   "prefill_ceiling_tflops": pre_ceiling,
+                   "prefill_ceiling_bound": "tensor" if tensor_peak <= hbm_ceiling else "hbm",
+                   "prefill_frac_of_ceiling": pre_tflops / pre_ceiling,
                    "decode_only_tokens_per_s": B * S / (decode_ms * 1e-3),
                    "input_generation_s": gen_s},
         "e2e": ({"value": B * S * e2e_steps * ws / (e2e_ms * 1e-3), "unit": UNIT,

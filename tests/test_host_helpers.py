@@ -2,7 +2,8 @@
 import numpy as np
 
 from h2o_parity import _slots_of
-from workloads import bf16_bits_to_f32, decode_bytes_per_row_step, stream_chunk
+from workloads import (bf16_bits_to_f32, decode_bytes_per_row_step, prefill_bytes_per_row,
+                       prefill_flops_per_row, stream_chunk)
 
 
 def test_stream_chunks_are_reproducible_and_independent():
@@ -44,3 +45,20 @@ def test_decode_byte_model_of_the_layouts():
     # the ring layout reads h positions instead of k and moves one token (8d + 8)
     assert ring - slots == 4 * h - 4 * k + 8 * d + 8
     assert decode_bytes_per_row_step(k, d, "fp8") == 2 * k * d + 20 * k + 12 * d + 16
+
+
+def test_prefill_byte_and_flop_models():
+    """T = 4, d = 2, k = 3 by hand: Q, K, V read 3 * 4 * 2 * 2 = 48 bytes, fp32
+    O written 4 * 2 * 4 = 32, three kept slots of K + V (2 * 2 * 2 = 8) plus
+    position and score (8): 48. Causal pairs 4 * 5 / 2 = 10, 2 * 2 * 2 flops
+    each (QK^T and PV)."""
+    assert prefill_bytes_per_row(4, 2, 3) == 48 + 32 + 3 * (8 + 8)
+    # FP8 slots: 2 code bytes per element of K and V, two fp32 scales
+    assert prefill_bytes_per_row(4, 2, 3, "fp8") == 48 + 32 + 3 * (4 + 8 + 8)
+    # a prompt shorter than the budget keeps every token
+    assert prefill_bytes_per_row(2, 2, 3) == 24 + 16 + 2 * 16
+    assert prefill_flops_per_row(4, 2) == 10 * 8
+    # the OPT-6.7B-shaped layer sits above the ridge of a 1.9 PF/s, 6.8 TB/s
+    # part and the 512-token prompt below it
+    ai = lambda T, k: prefill_flops_per_row(T, 128) / prefill_bytes_per_row(T, 128, k)
+    assert ai(2048, 460) > 1907.5 / 6.8152 > ai(512, 204)

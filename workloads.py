@@ -214,3 +214,15 @@ def prefill_flops_per_row(T: int, d: int) -> int:
     """Algorithmic flops of causal prefill attention for one row: QK^T and PV
     over the T(T+1)/2 causal (query, key) pairs, 2d flops each."""
     return 2 * d * T * (T + 1)
+
+
+def prefill_bytes_per_row(T: int, d: int, k: int, kv: str = "bf16") -> int:
+    """Algorithmic HBM bytes of the prefill of one row: the least any
+    implementation moves. Reads: the prompt's Q, K and V (bf16, 6Td). Writes:
+    the fp32 attention output (4Td) and the min(T, k) kept cache slots -- K and
+    V (bf16 4d a slot; FP8 codes 2d plus two fp32 scales) with their position
+    and accumulated score (8). The column sums and the kept positions are
+    intermediates a fused design keeps on chip, so they are not counted."""
+    kept = min(T, k)
+    slot = 2 * d + 8 if kv == "fp8" else 4 * d
+    return 6 * T * d + 4 * T * d + kept * (slot + 8)
