@@ -185,11 +185,13 @@ def _peaks():
 DECODE_SOURCES = ("decode.cu", "decode_kernel.cuh")  # the per-step decode kernel's source
 
 
-def _profiled_traffic(kernel_files, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
-    current source of the kernel (the sha256 of its files, concatenated in
-    order, is recorded in the summary)."""
-    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}.md")
+def _profiled_traffic(kernel_files, workload: str, rows: int, root: str = ROOT):
+    """DRAM bytes per launch of `rows` rows from a committed ncu summary, if it
+    was taken on the current source of the kernel (the sha256 of its files,
+    concatenated in order, is recorded in the summary). The summary states the
+    rows its figure is for; a row reads only its own cache, so the traffic is
+    scaled in proportion to the rows."""
+    path = os.path.join(root, "profiles", f"decode_kernel_{workload}.md")
     try:
         txt = open(path).read()
     except OSError:
@@ -198,11 +200,12 @@ def _profiled_traffic(kernel_files, workload: str):
     b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     if not (m and b):
         return None
-    src = b"".join(open(os.path.join(ROOT, "h2o_heavy_hitter_gb300", "csrc", f), "rb").read()
+    src = b"".join(open(os.path.join(root, "h2o_heavy_hitter_gb300", "csrc", f), "rb").read()
                    for f in kernel_files)
     if hashlib.sha256(src).hexdigest() != m.group(1):
         return None
-    return float(b.group(1))
+    r = re.search(r"traffic_rows:\s*([0-9]+)", txt)
+    return float(b.group(1)) * (rows / int(r.group(1)) if r else 1.0)
 
 
 def _dist_env():
@@ -601,7 +604,7 @@ def run_ours(args, w):
     tokens = B * S * args.steps * ws
     value = tokens / (elapsed_ms * 1e-3)
     roof = {"kernel": "h2o decode_kernel", "bound": "hbm", "peak": hbm, "unit": "GB/s",
-            "traffic": (_profiled_traffic(DECODE_SOURCES, w.name)
+            "traffic": (_profiled_traffic(DECODE_SOURCES, w.name, rows)
                         if args.kv == "bf16" and args.layout == "slots" else None),
             "bytes_per_launch": bytes_per_launch, "peak_source": f"{peak_kind} hbm_gbs"}
     if cycled_ms is not None:

@@ -62,3 +62,27 @@ def test_prefill_byte_and_flop_models():
     # part and the 512-token prompt below it
     ai = lambda T, k: prefill_flops_per_row(T, 128) / prefill_bytes_per_row(T, 128, k)
     assert ai(2048, 460) > 1907.5 / 6.8152 > ai(512, 204)
+
+
+def test_profiled_traffic_needs_the_current_source_and_scales_by_rows(tmp_path):
+    """The bench takes a kernel's DRAM traffic from a committed summary only if
+    the summary's source hash is that of the kernel's files now, and scales it
+    from the rows the summary states to the rows of the launch."""
+    import hashlib
+
+    import bench
+    csrc = tmp_path / "h2o_heavy_hitter_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "a.cu").write_bytes(b"one")
+    (csrc / "b.cuh").write_bytes(b"two")
+    digest = hashlib.sha256(b"onetwo").hexdigest()
+    summary = tmp_path / "profiles" / "decode_kernel_w.md"
+    summary.write_text(f"source_sha256 (a + b): {digest}\ndram_bytes_per_launch: 1000\n"
+                       "traffic_rows: 8\n")
+    files = ("a.cu", "b.cuh")
+    assert bench._profiled_traffic(files, "w", 8, str(tmp_path)) == 1000
+    assert bench._profiled_traffic(files, "w", 2, str(tmp_path)) == 250
+    assert bench._profiled_traffic(files, "other", 8, str(tmp_path)) is None
+    (csrc / "b.cuh").write_bytes(b"changed")
+    assert bench._profiled_traffic(files, "w", 8, str(tmp_path)) is None
