@@ -4,7 +4,8 @@ the library instead of an allocation).
 
 It is called through the C ABI twice in a row, on different shapes and data,
 and each time compared with h2o_prefill_attention (which allocates its scratch)
-using the same tolerances as the other prefill parity tests. A request larger
+using the same tolerances as the other prefill parity tests; a third call is
+compared with the CPU oracle directly, row by row. A request larger
 than the fixed scratch must be refused with H2O_EINVAL, and the call must run
 on the stream it is given, not on the caller's current stream. This file is
 named so that pytest collects it last; it also passes when run on its own.
@@ -15,7 +16,8 @@ import numpy as np
 import pytest
 import torch
 
-from workloads import Workload, head_direction, row_tokens
+import oracle
+from workloads import Workload, bf16_bits_to_f64, head_direction, row_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -72,6 +74,26 @@ def test_noalloc_matches_allocating_entry_point_on_two_calls():
     # the first call's values, which must not leak into this result
     Q, K, V = _inputs(291, 1, 4, 64, 700)
     _compare(_call_noalloc(lib, Q, K, V), h2o.h2o_prefill_attention(Q, K, V))
+
+
+def test_noalloc_matches_oracle():
+    """Every row's output and column sums against the fp64 oracle (the same
+    bar as the allocating entry point's oracle test): 3 x 2 rows of 389 tokens,
+    d = 128, three full query tiles and a ragged tail."""
+    _, lib = _lib()
+    w = Workload(293, "noalloc-oracle", 1, 3, 2, 128, 389, 0, 8, 8, 0.8)
+    bits = [row_tokens(w, 0, b, j, head_direction(w, 0, j))
+            for b in range(w.batch) for j in range(w.heads)]
+    Q, K, V = _inputs(293, 3, 2, 128, 389)
+    out, score = _call_noalloc(lib, Q, K, V)
+    torch.cuda.synchronize()
+    out, score = out.cpu().numpy(), score.cpu().numpy()
+    for i, x in enumerate(bits):
+        q, k, v = (bf16_bits_to_f64(y) for y in x)
+        O, colsum, _ = oracle.prefill_attention(q, k, v, oracle.default_scale(w.head_dim))
+        err = np.abs(out[i] - O)
+        assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (i, err.max(), err.mean())
+        np.testing.assert_allclose(score[i], colsum, rtol=SCORE_RTOL, atol=SCORE_ATOL)
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch():
