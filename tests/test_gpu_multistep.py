@@ -92,6 +92,50 @@ def test_multistep_equals_single_steps_bitwise(kv):
     many.close()
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("B,H,k", [(8, 32, 48), (40, 32, 48), (1, 4, 600)],
+                         ids=["256-rows", "1280-rows", "4-rows-split"])
+def test_back_to_back_steps_equal_synchronised_steps(kv, B, H, k):
+    """A decode step is launched as a programmatic dependent of the kernel
+    before it: its CTAs start (and prefetch the row's K/V into L2) while the
+    previous step, or an h2o_decode_steps call, of the same layer still runs.
+    Steps launched back to back after a multi-step call must equal, bit for
+    bit, the same calls with the stream synchronised after every launch. Row
+    shapes: 256 and 1280 rows of 48 slots (one CTA per row, 256 and 128
+    threads) and 4 rows of 600 slots split over several CTAs."""
+    import h2o_heavy_hitter_gb300 as h2o
+    d, h = 128, k // 2
+    r = k - h
+    T, S1, S2 = k + 40, 6, 40
+    w = Workload(440 + B + k, "pdl", 1, B, H, d, T, S1 + S2, h, r, 0.8)
+    dh = [head_direction(w, 0, j) for j in range(H)]
+    bits = [row_tokens(w, 0, b, j, dh[j]) for b in range(B) for j in range(H)]
+    full = [_bf16(np.stack([x[c] for x in bits])).reshape(B, H, T + S1 + S2, d) for c in range(3)]
+    pre = [x[:, :, :T].contiguous() for x in full]
+    steps = [x[:, :, T:].permute(2, 0, 1, 3).contiguous() for x in full]  # [S1 + S2, B, H, d]
+    outs, caches = [], []
+    for sync in (False, True):
+        ctx = h2o.h2o_create(1, B, H, d, h, r, kv=kv)
+        h2o.h2o_prefill(ctx, 0, *pre)
+        if sync:
+            torch.cuda.synchronize()
+        o = torch.zeros((S1 + S2, B, H, d), dtype=torch.float32, device="cuda")
+        h2o.h2o_decode_steps(ctx, 0, *[x[:S1] for x in steps], o[:S1])
+        for s in range(S1, S1 + S2):
+            if sync:
+                torch.cuda.synchronize()
+            h2o.h2o_decode_step(ctx, 0, steps[0][s], steps[1][s], steps[2][s], o[s])
+        h2o.h2o_sync_check(ctx)
+        view = h2o.h2o_cache_view(ctx, 0)
+        caches.append({key: view[key].clone() for key in ("score", "pos", "meta", "K", "V")})
+        outs.append(o)
+        ctx.close()
+    assert torch.equal(outs[0], outs[1])
+    for key in caches[0]:
+        assert torch.equal(caches[0][key], caches[1][key]), key
+    assert (caches[0]["meta"][:, 2] >= 0).any()  # evictions happened
+
+
 def test_multistep_zero_steps_and_state_errors():
     import h2o_heavy_hitter_gb300 as h2o
     ctx = h2o.h2o_create(1, 1, 2, 64, 4, 4)
