@@ -116,10 +116,22 @@ bool tma_aligned(const void* a, const void* b, const void* c, const void* d) {
   return ok(a) && ok(b) && ok(c) && ok(d);
 }
 
+// A context's memory lives on the device that was current when it was
+// created; its work must be enqueued there.
+int check_device(const h2o_ctx* c) {
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (cur != c->device)
+    return fail(H2O_EINVAL, "the context belongs to device " + std::to_string(c->device) +
+                                " but device " + std::to_string(cur) + " is current");
+  return H2O_OK;
+}
+
 int check_layer(const h2o_ctx* c, int layer) {
   if (!c) return fail(H2O_EINVAL, "null context");
   if (layer < 0 || layer >= c->layers) return fail(H2O_EINVAL, "layer out of range");
-  return H2O_OK;
+  return check_device(c);
 }
 
 int run_attention(const void* Q, const void* K, const void* V, int rows, int T,
@@ -493,6 +505,7 @@ int h2o_decode_steps(h2o_ctx* c, int layer, int steps, const void* q, const void
 int h2o_reset(h2o_ctx* c, int layer) {
   if (!c) return fail(H2O_EINVAL, "null context");
   if (layer < -1 || layer >= c->layers) return fail(H2O_EINVAL, "layer out of range");
+  if (int rc = check_device(c)) return rc;
   const int l0 = layer < 0 ? 0 : layer, l1 = layer < 0 ? c->layers : layer + 1;
   cudaStream_t s = current_stream();
   for (int l = l0; l < l1; ++l) {
@@ -554,6 +567,7 @@ int h2o_cache_dims(h2o_ctx* c, int* k, int* rows) {
 
 int h2o_test_wait_limit(h2o_ctx* c) {
   if (!c) return fail(H2O_EINVAL, "null context");
+  if (int rc = check_device(c)) return rc;
   cudaError_t e = h2o::wait_limit_probe(c->err, current_stream());
   if (e != cudaSuccess) return cuda_fail(e, "wait-limit probe launch");
   return H2O_OK;
@@ -561,6 +575,7 @@ int h2o_test_wait_limit(h2o_ctx* c) {
 
 int h2o_sync_check(h2o_ctx* c) {
   if (!c) return fail(H2O_EINVAL, "null context");
+  if (int rc = check_device(c)) return rc;
   return check_error_word(c->err, current_stream());
 }
 

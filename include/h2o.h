@@ -18,7 +18,9 @@
  *     that give up set a device error word that h2o_sync_check() reports.
  *   - Device pointers are CUDA device addresses on the current device; host
  *     pointers are ordinary CPU memory. Every buffer passed in stays owned by
- *     the caller and is only accessed by work the call enqueues.
+ *     the caller and is only accessed by work the call enqueues. A context
+ *     belongs to the device that was current when it was created: an entry
+ *     point given a context returns H2O_EINVAL while another device is current.
  *   - All device work is enqueued, asynchronously, on the calling thread's
  *     current PyTorch CUDA stream (c10::cuda::getCurrentCUDAStream()). The
  *     caller must have initialised PyTorch's CUDA state on that device
