@@ -292,8 +292,12 @@ cudaError_t prefill_select(const float* colsum, int rows, int T, const int32_t* 
                            int h, int r, bool ring, float* score, int32_t* pos, int32_t* meta,
                            int32_t* err, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  select_kernel<<<rows, kSelectThreads, 0, stream>>>(colsum, T, lens, heads, h, r, h + r, ring,
-                                                     score, pos, meta, err);
+  // About four candidates per thread: a short prompt's row takes a small block,
+  // so that many rows run at once (the result does not depend on the block
+  // size: compaction and ties follow position order).
+  const int threads = std::min(kSelectThreads, std::max(128, ((T + 3) / 4 + 31) / 32 * 32));
+  select_kernel<<<rows, threads, 0, stream>>>(colsum, T, lens, heads, h, r, h + r, ring, score,
+                                              pos, meta, err);
   return cudaGetLastError();
 }
 
