@@ -185,6 +185,10 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const float* __r
   }
 }
 
+// One warp per kGatherSlots slots: every lane loads its 16-byte chunks of all
+// of them before it stores any, so that several loads per lane are in flight.
+constexpr int kGatherSlots = 4;
+
 template <int D>
 __global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __restrict__ K,
                                                     const __nv_bfloat16* __restrict__ V, int T,
@@ -192,25 +196,38 @@ __global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __rest
                                                     __nv_bfloat16* __restrict__ Kc,
                                                     __nv_bfloat16* __restrict__ Vc,
                                                     int32_t* __restrict__ err) {
-  constexpr int CH = D / 8;  // 16-byte chunks per row
+  constexpr int CH = D / 8;                    // 16-byte chunks per K or V row
+  constexpr int PER_SLOT = 2 * CH;             // chunks of a slot: K row, then V row
+  constexpr int N = PER_SLOT * kGatherSlots / 32;  // chunks per lane
   const int row = blockIdx.x;
-  const int slot = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int slot0 = (blockIdx.y * 8 + (threadIdx.x >> 5)) * kGatherSlots;
   const int lane = threadIdx.x & 31;
-  if (slot >= k) return;
-  const int p = pos[static_cast<size_t>(row) * k + slot];
-  if (p < 0) return;
-  if (p >= T) {  // never written by the selection; reported, nothing is read
-    if (lane == 0 && err) atomicOr(err, kErrBadState);
-    return;
+  uint4 v[N];
+  size_t dst[N];
+  bool isv[N], live[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const int q = lane + 32 * i;
+    const int slot = slot0 + q / PER_SLOT;
+    const int c = q % PER_SLOT;
+    isv[i] = c >= CH;
+    live[i] = false;
+    if (slot >= k) continue;
+    const int p = pos[static_cast<size_t>(row) * k + slot];
+    if (p < 0) continue;
+    if (p >= T) {  // never written by the selection; reported, nothing is read
+      if (c == 0 && err) atomicOr(err, kErrBadState);
+      continue;
+    }
+    const int cc = isv[i] ? c - CH : c;
+    v[i] = *reinterpret_cast<const uint4*>((isv[i] ? V : K) +
+                                           (static_cast<size_t>(row) * T + p) * D + cc * 8);
+    dst[i] = (static_cast<size_t>(row) * k + slot) * D + cc * 8;
+    live[i] = true;
   }
-  const size_t src = (static_cast<size_t>(row) * T + p) * D;
-  const size_t dst = (static_cast<size_t>(row) * k + slot) * D;
-  for (int c = lane; c < 2 * CH; c += 32) {
-    const bool isv = c >= CH;
-    const int cc = isv ? c - CH : c;
-    const uint4 v = *reinterpret_cast<const uint4*>((isv ? V : K) + src + cc * 8);
-    *reinterpret_cast<uint4*>((isv ? Vc : Kc) + dst + cc * 8) = v;
-  }
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    if (live[i]) *reinterpret_cast<uint4*>((isv[i] ? Vc : Kc) + dst[i]) = v[i];
 }
 
 // E4M3 cache: one warp per slot quantises the kept token's K and V rows
@@ -305,7 +322,8 @@ cudaError_t prefill_gather(const void* K, const void* V, int rows, int T, int d,
                            const int32_t* pos, void* Kc, void* Vc, int32_t* err,
                            cudaStream_t stream) {
   if (rows == 0 || T == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>((k + 7) / 8));
+  const int per_block = 8 * kGatherSlots;
+  const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>((k + per_block - 1) / per_block));
   auto kk = static_cast<const __nv_bfloat16*>(K);
   auto vv = static_cast<const __nv_bfloat16*>(V);
   auto kc = static_cast<__nv_bfloat16*>(Kc);
