@@ -230,8 +230,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __rest
     if (live[i]) *reinterpret_cast<uint4*>((isv[i] ? Vc : Kc) + dst[i]) = v[i];
 }
 
-// E4M3 cache: one warp per slot quantises the kept token's K and V rows
-// (D / 32 values per lane) with one scale each.
+// E4M3 cache: eight lanes per slot, four slots per warp; every lane loads its
+// D / 8 values of the kept token's K and V rows, then each row is quantised
+// with one scale (the amax is reduced over the slot's eight lanes).
 template <int D>
 __global__ void __launch_bounds__(256) gather_fp8_kernel(const __nv_bfloat16* __restrict__ K,
                                                         const __nv_bfloat16* __restrict__ V, int T,
@@ -241,33 +242,46 @@ __global__ void __launch_bounds__(256) gather_fp8_kernel(const __nv_bfloat16* __
                                                         float* __restrict__ kscale,
                                                         float* __restrict__ vscale,
                                                         int32_t* __restrict__ err) {
-  constexpr int EPL = D / 32;  // values per lane: 4 (d = 128) or 2 (d = 64)
+  constexpr int LPS = 8;          // lanes per slot
+  constexpr int EPL = D / LPS;    // values per lane: 16 (d = 128) or 8 (d = 64)
+  constexpr int NV = EPL / 8;     // 16-byte loads per lane and row
   const int row = blockIdx.x;
-  const int slot = blockIdx.y * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (slot >= k) return;  // whole warps leave together: the shuffles below see full warps
+  const int slot = (blockIdx.y * 8 + (threadIdx.x >> 5)) * kGatherSlots + lane / LPS;
+  const int l = lane % LPS;
+  const unsigned gmask = 0xffu << (lane & ~(LPS - 1));  // the slot's eight lanes
+  // The eight lanes of a slot share slot and position, so they leave together
+  // and the quantiser's shuffles below see whole groups.
+  if (slot >= k) return;
   const int p = pos[static_cast<size_t>(row) * k + slot];
   if (p < 0) return;
   if (p >= T) {  // never written by the selection; reported, nothing is read
-    if (lane == 0 && err) atomicOr(err, kErrBadState);
+    if (l == 0 && err) atomicOr(err, kErrBadState);
     return;
   }
-  const size_t src = (static_cast<size_t>(row) * T + p) * D + lane * EPL;
-  const size_t dst = (static_cast<size_t>(row) * k + slot) * D + lane * EPL;
+  const size_t src = (static_cast<size_t>(row) * T + p) * D + l * EPL;
+  const size_t dst = (static_cast<size_t>(row) * k + slot) * D + l * EPL;
+  uint4 raw[2][NV];
+#pragma unroll
+  for (int isv = 0; isv < 2; ++isv)
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+      raw[isv][j] = *reinterpret_cast<const uint4*>((isv ? V : K) + src + 8 * j);
 #pragma unroll
   for (int isv = 0; isv < 2; ++isv) {
-    const __nv_bfloat16* x = (isv ? V : K) + src;
     float f[EPL];
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) f[i] = __bfloat162float(x[i]);
+    for (int j = 0; j < NV; ++j) bf16x8_to_f32(raw[isv][j], f + 8 * j);
     uint32_t pairs[EPL / 2];
-    const float sc = quantize_e4m3<EPL>(f, 0xffffffffu, 32, pairs);
+    const float sc = quantize_e4m3<EPL>(f, gmask, LPS, pairs);
     uint8_t* out = (isv ? Vc : Kc) + dst;
-    if constexpr (EPL == 4)
-      *reinterpret_cast<uint32_t*>(out) = pairs[0] | (pairs[1] << 16);
+    if constexpr (EPL == 16)
+      *reinterpret_cast<uint4*>(out) =
+          make_uint4(pairs[0] | (pairs[1] << 16), pairs[2] | (pairs[3] << 16),
+                     pairs[4] | (pairs[5] << 16), pairs[6] | (pairs[7] << 16));
     else
-      *reinterpret_cast<uint16_t*>(out) = static_cast<uint16_t>(pairs[0]);
-    if (lane == 0) (isv ? vscale : kscale)[static_cast<size_t>(row) * k + slot] = sc;
+      *reinterpret_cast<uint2*>(out) = make_uint2(pairs[0] | (pairs[1] << 16), pairs[2] | (pairs[3] << 16));
+    if (l == 0) (isv ? vscale : kscale)[static_cast<size_t>(row) * k + slot] = sc;
   }
 }
 
@@ -339,7 +353,8 @@ cudaError_t prefill_gather_fp8(const void* K, const void* V, int rows, int T, in
                                const int32_t* pos, void* Kc, void* Vc, float* kscale,
                                float* vscale, int32_t* err, cudaStream_t stream) {
   if (rows == 0 || T == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>((k + 7) / 8));
+  const int per_block = 8 * kGatherSlots;
+  const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>((k + per_block - 1) / per_block));
   auto kk = static_cast<const __nv_bfloat16*>(K);
   auto vv = static_cast<const __nv_bfloat16*>(V);
   auto kc = static_cast<uint8_t*>(Kc);
