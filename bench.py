@@ -150,6 +150,12 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
+        return self.summarize(out)
+
+    def summarize(self, out: str):
+        """The clock record of nvidia-smi's CSV lines (FIELDS, no header, no
+        units): median and minimum SM clock and the throttle reasons seen,
+        over the samples inside the timed region when there are at least 3."""
         import datetime
         rows = []
         for line in out.strip().splitlines():

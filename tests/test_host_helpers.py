@@ -86,3 +86,31 @@ def test_profiled_traffic_needs_the_current_source_and_scales_by_rows(tmp_path):
     assert bench._profiled_traffic(files, "other", 8, str(tmp_path)) is None
     (csrc / "b.cuh").write_bytes(b"changed")
     assert bench._profiled_traffic(files, "w", 8, str(tmp_path)) is None
+
+
+def test_clock_record_keeps_the_timed_region_and_its_throttle_reasons():
+    import datetime
+
+    import bench
+    day = "2026/12/03 08:00:0"
+    na = "Not Active"
+
+    def line(sec, mhz, cap=False):
+        return (f"{day}{sec}.000, {mhz}, 2070, 900.0, 0x0, {na}, {na}, {na}, "
+                f"{'Active' if cap else na}")
+
+    text = "\n".join([line(0, 1200), line(2, 2070), line(3, 2070, cap=True), line(4, 2055),
+                      line(5, 2070), line(8, 1000, cap=True), "garbage,1,2"])
+    t = lambda sec: datetime.datetime.strptime(f"{day}{sec}.000", "%Y/%m/%d %H:%M:%S.%f").timestamp()
+    c = bench.ClockSampler(0)
+    c.mark(t(2), t(5))
+    rec = c.summarize(text)
+    assert rec["samples_in_timed_region"] == 4 and rec["window"] == "timed region"
+    assert rec["sm_mhz"] == 2070.0 and rec["sm_mhz_min"] == 2055.0 and rec["sm_max_mhz"] == 2070.0
+    assert rec["reasons"] == ["sw_power_cap"]
+    # fewer than three samples in the timed region: the whole window is reported
+    c.mark(t(8), t(9))
+    rec = c.summarize(text)
+    assert rec["window"] == "warm-up and timed region" and rec["samples"] == 6
+    assert rec["sm_mhz_min"] == 1000.0 and rec["reasons"] == ["sw_power_cap"]
+    assert c.summarize("") is None
